@@ -1,0 +1,212 @@
+/*
+ * oracle.c -- plain, slow CPU reference ("the oracle") for the DFlash2
+ * candidate-selector head.
+ *
+ * TEST INFRASTRUCTURE ONLY.  The tests, the package's smoke check and the
+ * benchmark's CPU-baseline / reference leg may load this library.  The product
+ * path (the CUDA library and its binding) never includes, links or calls it,
+ * and shares no code with it.
+ *
+ * What it computes, step by step, with no blocking, fusion or reordering
+ * beyond the definitions:
+ *
+ *  1. LM head.  logit[r,v] = sum_h hidden[r,h] * W_vocab[v,h].
+ *     "DFlash 2: Keep Drafting Parallel", section "A Lightweight Path
+ *     Selector": the unary term U_t(b) is the drafter's own logit.  Each
+ *     product of two bf16 values is exact in double; the sum runs in double
+ *     in increasing h and is rounded once to float32 (the float32 logits the
+ *     method's engines hand to top-k).
+ *  2. Top-k.  Full sort of each row by (logit desc, token id asc), first k.
+ *     "DFlash2 Lands in llama.cpp", section "What llama.cpp Actually Builds
+ *     for the Selector": candidates = top_k(logits); the unary scores are the
+ *     candidates' logits.  Ties go to the lower token id.
+ *  3. Gate.  g[r,d] = sum_h W_sel[d,h] * hidden[r,h], in double, linear with
+ *     no bias: the hidden state of the current position projected through the
+ *     selector projection (same section of the llama.cpp page; "context gate
+ *     H(h_t)" on the DFlash 2 page).
+ *  4. Lattice.  For position r = b*T + t, predecessor candidates are the
+ *     previous position's candidates, or the anchor (last verified token) at
+ *     t = 0; S[r,i,j] = U[r,j] + sum_d (A[prev_i,d] * g[r,d]) * B[cand_j,d]
+ *     (DFlash 2 page, equation S_t(a,b) = U_t(b) + <A(a) (.) H(h_t), B(b)>;
+ *     llama.cpp page, section "The Central Insight": edge = unary + pairwise).
+ *     Computed in double, rounded once to float32.
+ *  5. Packing.  Row r = [k candidate ids as exact floats | S[r,i,j] with the
+ *     predecessor index i major] (llama.cpp page: each row holds the candidate
+ *     IDs followed by the transition scores).  At t = 0 every predecessor row
+ *     holds the anchor-conditioned scores.
+ *  6. Walk.  j_0 = argmax_j S[(b,0),0,j]; j_t = argmax_j S[(b,t),j_{t-1},j];
+ *     draft[b,t] = cand[(b,t), j_t]; the first maximum wins (llama.cpp page,
+ *     the predecessor = anchor walk; DFlash 2 page: greedy follows the best
+ *     successor at each step).  Decided on the float32 lattice.
+ *
+ * bf16 tensors are passed as their uint16 bit patterns.  Every function
+ * returns 0 on success and a negative code on bad arguments or non-finite
+ * values.  Build: gcc -O2 -fopenmp -ffp-contract=off (no fused multiply-add,
+ * so x86 and Arm give the same bits).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Step 1: float32 logits (double accumulation, one rounding).  logits64 may be NULL. */
+int oracle_logits(const uint16_t *hidden, const uint16_t *W_vocab, int64_t R, int64_t H, int64_t V,
+                  float *logits, double *logits64)
+{
+    if (!hidden || !W_vocab || !logits || R < 0 || H <= 0 || V <= 0)
+        return -1;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t v = 0; v < V; ++v) {
+            const uint16_t *hr = hidden + r * H;
+            const uint16_t *wv = W_vocab + v * H;
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                acc += bf16_to_double(hr[h]) * bf16_to_double(wv[h]);
+            logits[r * V + v] = (float)acc;
+            if (logits64)
+                logits64[r * V + v] = acc;
+        }
+    }
+    return 0;
+}
+
+typedef struct {
+    float value;
+    int32_t id;
+} scored_token;
+
+/* (value desc, id asc): a strict total order on distinct ids. */
+static int by_value_desc_id_asc(const void *pa, const void *pb)
+{
+    const scored_token *a = (const scored_token *)pa;
+    const scored_token *b = (const scored_token *)pb;
+    if (a->value > b->value)
+        return -1;
+    if (a->value < b->value)
+        return 1;
+    return (a->id < b->id) ? -1 : (a->id > b->id) ? 1 : 0;
+}
+
+/* Step 2: top-k of each row by a full sort. */
+int oracle_topk(const float *logits, int64_t R, int64_t V, int32_t k, int32_t *ids, float *vals)
+{
+    if (!logits || !ids || !vals || R < 0 || V <= 0 || k < 1 || k > V)
+        return -1;
+    for (int64_t i = 0; i < R * V; ++i)
+        if (!isfinite(logits[i]))
+            return -2;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t r = 0; r < R; ++r) {
+        scored_token *row = (scored_token *)malloc((size_t)V * sizeof *row);
+        if (!row) {
+            bad |= 1;
+            continue;
+        }
+        for (int64_t v = 0; v < V; ++v) {
+            row[v].value = logits[r * V + v];
+            row[v].id = (int32_t)v;
+        }
+        qsort(row, (size_t)V, sizeof *row, by_value_desc_id_asc);
+        for (int32_t j = 0; j < k; ++j) {
+            ids[r * k + j] = row[j].id;
+            vals[r * k + j] = row[j].value;
+        }
+        free(row);
+    }
+    return bad ? -3 : 0;
+}
+
+/* Step 3: gate in double. */
+int oracle_gate(const uint16_t *hidden, const uint16_t *W_sel, int64_t R, int64_t H, int64_t D, double *gate)
+{
+    if (!hidden || !W_sel || !gate || R < 0 || H <= 0 || D <= 0)
+        return -1;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int64_t h = 0; h < H; ++h)
+                acc += bf16_to_double(W_sel[d * H + h]) * bf16_to_double(hidden[r * H + h]);
+            gate[r * D + d] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Steps 4-5: packed lattice rows, float32 [B*T, k + k*k]; lattice64 (may be
+ * NULL) receives the unrounded double scores [B*T, k*k].
+ */
+int oracle_lattice(int64_t B, int64_t T, int32_t k, int64_t V, int64_t D, const int32_t *cand_ids,
+                   const float *unary, const double *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
+                   const int32_t *anchor, float *lattice, double *lattice64)
+{
+    if (B < 0 || T <= 0 || k < 1 || V <= 0 || D <= 0 || !cand_ids || !unary || !gate || !pred_cb || !succ_cb ||
+        !anchor || !lattice)
+        return -1;
+    for (int64_t b = 0; b < B; ++b)
+        if (anchor[b] < 0 || anchor[b] >= V)
+            return -2;
+    for (int64_t i = 0; i < B * T * k; ++i)
+        if (cand_ids[i] < 0 || cand_ids[i] >= V)
+            return -2;
+    const int64_t width = (int64_t)k + (int64_t)k * k;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < T; ++t) {
+            const int64_t r = b * T + t;
+            float *row = lattice + r * width;
+            for (int32_t j = 0; j < k; ++j)
+                row[j] = (float)cand_ids[r * k + j];
+            for (int32_t i = 0; i < k; ++i) {
+                const int64_t prev = (t == 0) ? anchor[b] : cand_ids[(r - 1) * k + i];
+                for (int32_t j = 0; j < k; ++j) {
+                    const int64_t cand = cand_ids[r * k + j];
+                    double pairwise = 0.0;
+                    for (int64_t d = 0; d < D; ++d)
+                        pairwise += (bf16_to_double(pred_cb[prev * D + d]) * gate[r * D + d]) *
+                                    bf16_to_double(succ_cb[cand * D + d]);
+                    const double s = (double)unary[r * k + j] + pairwise;
+                    row[k + (int64_t)i * k + j] = (float)s;
+                    if (lattice64)
+                        lattice64[r * (int64_t)k * k + (int64_t)i * k + j] = s;
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Step 6: greedy walk on the packed float32 lattice.  choice (may be NULL) gets j_t. */
+int oracle_walk(int64_t B, int64_t T, int32_t k, const float *lattice, int32_t *draft, int32_t *choice)
+{
+    if (B < 0 || T <= 0 || k < 1 || !lattice || !draft)
+        return -1;
+    const int64_t width = (int64_t)k + (int64_t)k * k;
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t jprev = 0; /* position 0: every predecessor row holds the anchor's scores */
+        for (int64_t t = 0; t < T; ++t) {
+            const float *row = lattice + (b * T + t) * width;
+            const float *scores = row + k + (int64_t)jprev * k;
+            int32_t best = 0;
+            for (int32_t j = 1; j < k; ++j)
+                if (scores[j] > scores[best])
+                    best = j;
+            draft[b * T + t] = (int32_t)row[best];
+            if (choice)
+                choice[b * T + t] = best;
+            jprev = best;
+        }
+    }
+    return 0;
+}
