@@ -1,0 +1,378 @@
+#!/usr/bin/env python3
+"""Benchmark of the DFlash2 candidate-selector head on GB300.
+
+One step = one dflash2_select call over a whole draft block: LM head with fused
+top-k, gate, k x k lattice and greedy walk for every sequence of the workload
+(default: the 8B-class drafter head at batch 1, B=1 T=16 H=4096 V=151936 k=8
+D=256).  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Multi-GPU: launched one process per GPU (torchrun); every rank runs an
+independent replica of the workload (sequences shard with no exchange step),
+so scaling is weak and the value is the rows of all ranks over the slowest
+rank's time.  --impl reference times the CPU oracle (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from speculative_decoding_drafter_gb300.synth import CONFIGS, make_inputs  # noqa: E402
+
+METRIC = "selector draft rows/s and µs/block; % of HBM or bf16 tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+LAUNCHES_PER_STEP = 5  # LM head + top-k, gate, merge, lattice, walk
+DOMINANT_SOURCES = ["speculative_decoding_drafter_gb300/csrc/gemm_tc.cu", "speculative_decoding_drafter_gb300/csrc/ptx.cuh",
+                    "speculative_decoding_drafter_gb300/csrc/topk.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="8b_b1", choices=list(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if a.steps < 1:
+        ap.error("--steps must be at least 1")
+    return a
+
+
+def workload_name(cfg) -> str:
+    return f"{cfg.name}: B={cfg.B} T={cfg.T} H={cfg.H} V={cfg.V} k={cfg.k} D={cfg.D}"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            return json.load(fh), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_bound(cfg, peaks):
+    t_hbm = cfg.V * cfg.H * 2 / (peaks["hbm_gbs"] * 1e9)
+    t_tc = 2.0 * cfg.R * cfg.H * cfg.V / (peaks["bf16_tflops"] * 1e12)
+    return "hbm" if t_hbm >= t_tc else "tensor"
+
+
+def dominant_source_sha() -> str:
+    h = hashlib.sha256()
+    for rel in DOMINANT_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(cfg):
+    """DRAM bytes per LM-head launch from the committed ncu summary, if it matches this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as fh:
+        rec = json.load(fh)
+    ent = rec.get(cfg.name)
+    if not ent or ent.get("source_sha") != dominant_source_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.device_id = device_id
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.device_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [ln.strip().split(", ") for ln in self.tmp.read().splitlines() if ln.strip()]
+        self.tmp.close()
+        os.unlink(self.tmp.name)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t_first: int):
+        """Median SM clock and the throttle reasons seen in the samples after t_first (skip the lead-in)."""
+        rows = rows[t_first:] or rows
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[4:8]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def device_id_for_smi(torch) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+        return vis or "0"
+
+
+def time_oracle_rows(cfg, x, rows_per_step: int, step: int):
+    """Run the oracle on the first rows_per_step positions of one sequence; returns seconds."""
+    import oracle
+
+    b = step % cfg.B
+    rows = np.arange(b * cfg.T, b * cfg.T + rows_per_step)
+    t0 = time.perf_counter()
+    oracle.select(x["hidden"][rows], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"][b:b + 1],
+                  cfg.k, rows_per_step)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(cfg, x, budget_s: float = 20.0):
+    """The oracle, as it stands, timed on a bounded sample of the workload (whole sequences if they fit)."""
+    import oracle
+
+    t_row = time_oracle_rows(cfg, x, 1, 0)
+    n_rows = int(max(1, min(cfg.T, budget_s / max(t_row, 1e-9))))
+    t = time_oracle_rows(cfg, x, n_rows, 0)
+    return {"value": n_rows / t, "unit": "rows/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"sequence 0, positions 0..{n_rows - 1} of {cfg.T} (full vocabulary, full pipeline), one run"}
+
+
+def run_reference(args, cfg, rank: int):
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    x = make_inputs(cfg, 0)
+    t_row = time_oracle_rows(cfg, x, 1, 0)
+    budget = 150.0 / (args.steps + args.warmup)
+    rows_per_step = int(max(1, min(cfg.T, budget / max(t_row, 1e-9))))
+    for w in range(args.warmup):
+        time_oracle_rows(cfg, x, rows_per_step, w)
+    total = 0.0
+    for s in range(args.steps):
+        total += time_oracle_rows(cfg, x, rows_per_step, s)
+    value = rows_per_step * args.steps / total
+    sample = (f"per step: sequence (step mod B), positions 0..{rows_per_step - 1} of {cfg.T}, full vocabulary, "
+              f"full oracle pipeline")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; stands in for the pages' GSM8K/MATH-500/HumanEval/MBPP/MT-Bench drafter states)",
+        "config": {"workload": workload_name(cfg), "sample_rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": oracle.threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, cfg, rank: int, world: int):
+    import torch
+
+    from speculative_decoding_drafter_gb300 import dflash2 as df
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    df.library()
+    peaks, peak_kind = load_peaks()
+
+    x = make_inputs(cfg, 0)
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    d = {n: dev_bf16(x[n]) for n in ("hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb")}
+    d["anchor"] = torch.from_numpy(x["anchor"]).cuda()
+    R, k = cfg.R, cfg.k
+    lattice = torch.empty((R, k + k * k), dtype=torch.float32, device="cuda")
+    draft = torch.empty((cfg.B, cfg.T), dtype=torch.int32, device="cuda")
+    ws = df.Workspace(df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, k, cfg.D))
+
+    def step():
+        df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], d["anchor"], k, cfg.T,
+                          lattice=lattice, draft_ids=draft, workspace=ws)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    df.dflash2_check_device_status(ws)
+
+    # ---- device-timed region: K steps, LM-head launches bracketed by their own events
+    K = args.steps
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device_id_for_smi(torch)) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    start.record()
+    for i in range(K):
+        df.dflash2_profile_events(eb[i], ee[i])
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    df.dflash2_profile_events(None, None)
+    clock_rows = sampler.stop() if sampler else []
+    df.dflash2_check_device_status(ws)
+    ms = start.elapsed_time(end)
+    lm_ms = sum(eb[i].elapsed_time(ee[i]) for i in range(K)) / K
+    if dist is not None:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end-to-end through the public API with host buffers (pinned), per-step sync
+    e2e = None
+    if not args.no_e2e:
+        h_hidden = torch.from_numpy(x["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        h_anchor = torch.from_numpy(x["anchor"]).pin_memory()
+        h_lat = torch.empty_like(lattice, device="cpu").pin_memory()
+        h_draft = torch.empty_like(draft, device="cpu").pin_memory()
+
+        def e2e_step():
+            d["hidden"].copy_(h_hidden, non_blocking=True)
+            d["anchor"].copy_(h_anchor, non_blocking=True)
+            step()
+            h_draft.copy_(draft, non_blocking=True)
+            h_lat.copy_(lattice, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(args.warmup):
+            e2e_step()
+        barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record()
+        for _ in range(K):
+            e2e_step()
+        s1.record()
+        torch.cuda.synchronize()
+        e_ms = s0.elapsed_time(s1)
+        if dist is not None:
+            t = torch.tensor([e_ms], dtype=torch.float64, device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        h2d = h_hidden.numel() * 2 + h_anchor.numel() * 4
+        d2h = h_lat.numel() * 4 + h_draft.numel() * 4
+        e2e = {"value": world * R * K / (e_ms / 1e3), "unit": "rows/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K, "sync": "per step"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    bound = roofline_bound(cfg, peaks)
+    lm_s = lm_ms / 1e3
+    if bound == "hbm":
+        algo = cfg.V * cfg.H * 2 + cfg.R * cfg.H * 2
+        achieved, peak, unit = algo / lm_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        algo = 2.0 * cfg.R * cfg.H * cfg.V
+        achieved, peak, unit = algo / lm_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": recorded_traffic(cfg), "kernel": "gemm_tc_kernel (LM head + fused top-k)",
+            "kernel_us": lm_ms * 1e3, "algorithmic_per_launch": algo, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)"
+            if peak_kind == "measured" else "fallback"}
+    # the same roofline over the whole step (every launch of the call, host gaps included)
+    roof["step_frac"] = (lm_ms / (ms / K)) * roof["frac"]
+
+    clocks = ClockSampler.summarize(clock_rows, 0) if clock_rows else {"sm_mhz": None, "sm_max_mhz": None,
+                                                                        "reasons": ["no samples"], "samples": 0}
+    line = {
+        "impl": "ours", "metric": METRIC, "value": world * R * K / (ms / 1e3), "unit": "rows/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "us_per_block": 1e3 * ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; stands in for the pages' GSM8K/MATH-500/HumanEval/MBPP/MT-Bench drafter states)",
+        "config": {"workload": workload_name(cfg),
+                   "l2": f"inputs larger than L2 (W_vocab {cfg.V * cfg.H * 2 / 1e9:.2f} GB vs 129 MB L2)"
+                   if cfg.V * cfg.H * 2 > 129e6 else "inputs fit in L2 (warm)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "gpu_launches": LAUNCHES_PER_STEP * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, x)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    cfg = CONFIGS[args.config]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    if args.impl == "reference":
+        return run_reference(args, cfg, rank)
+    return run_ours(args, cfg, rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,176 @@
+/*
+ * dflash2.h -- C ABI of the DFlash2 candidate-selector head for GB300 (sm_103a).
+ *
+ * The selector head turns a block of drafter hidden states into a draft
+ * block.  For every draft position t of every sequence b (row r = b*T + t):
+ *
+ *   logits_r   = W_vocab . h_r                      LM head (float32 accumulate)
+ *   cand_r, U_r = top-k of logits_r                  ties: lower token id first
+ *   g_r        = W_sel . h_r                         selector gate (linear, no bias)
+ *   S_r[i][j]  = U_r[j] + < A(prev_i) (.) g_r , B(cand_r[j]) >
+ *                prev = cand_{r-1} for t > 0, the anchor token for t = 0
+ *   draft      = greedy walk: j_0 = argmax_j S_(b,0)[0][j],
+ *                j_t = argmax_j S_(b,t)[j_(t-1)][j], emit cand[j_t]
+ *
+ * Sources: "DFlash 2: Keep Drafting Parallel" (inco.ai), section "A
+ * Lightweight Path Selector" (the score S_t(a,b) = U_t(b) + <A(a) (.) H(h_t),
+ * B(b)>, the top-16 candidates, the rank-256 codebooks A and B, greedy from
+ * the last verified token); "DFlash2 Lands in llama.cpp: What PR #27342
+ * Actually Changes", sections "The Central Insight" (edge = unary +
+ * pairwise) and "What llama.cpp Actually Builds for the Selector"
+ * (candidates = top_k(logits), the gathered unary scores, the selector hidden
+ * projection, the predecessor/successor codebook gathers, rows packed as
+ * candidate ids followed by transition scores, and the walk that starts with
+ * predecessor = anchor).
+ *
+ * Conventions shared by every entry point:
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
+ *    library allocates nothing, frees nothing, and never synchronises a
+ *    stream (except dflash2_check_device_status, which says so).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  The returned status covers argument
+ *    validation and launch errors (cudaGetLastError after enqueue); it does
+ *    not wait for the kernels.
+ *  - bf16 tensors are IEEE bfloat16, row-major and contiguous.  Tensors read
+ *    by the tensor-memory-accelerator or by 16-byte vector loads (hidden,
+ *    W_vocab, W_sel, pred_cb, succ_cb, logits) must be 16-byte aligned; the
+ *    workspace must be 256-byte aligned; every other pointer 4-byte aligned.
+ *  - Limits: B >= 1, T >= 1, 1 <= k <= 32 and k <= V, V < 2^24 (candidate
+ *    ids are stored as exact floats in the lattice), H >= 8 and H % 8 == 0,
+ *    8 <= D <= 1024 and D % 8 == 0, B*T <= 2^20.  Outside them a call returns
+ *    DF2_ERR_INVALID_ARG (malformed) or DF2_ERR_UNSUPPORTED (well formed but
+ *    beyond what the kernels implement) and enqueues nothing.
+ *  - anchor values and W-row indices must lie in [0, V); this is a
+ *    precondition (out-of-range anchors are clamped to 0 on the device so
+ *    that no read leaves the codebooks, and the result is then unspecified).
+ *  - Hidden rows are already aligned to the draft positions: row b*T + t
+ *    scores draft position t of sequence b (the export slices the seed
+ *    position off upstream; "How to Convert and Run DFlash Models with
+ *    OpenVINO", defect 1 of "Three ways ...").
+ *
+ * Packed lattice row r (float32, width k + k*k):
+ *    [ cand_0 .. cand_{k-1} | S[0][0..k-1] | S[1][0..k-1] | ... | S[k-1][0..k-1] ]
+ *  candidate ids are stored as exact float values; S is predecessor-major.
+ *  At t = 0 the single predecessor is the anchor and all k predecessor rows
+ *  hold the same anchor-conditioned scores; the walk reads row 0.
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define DF2_API __attribute__((visibility("default")))
+#else
+#define DF2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum df2_status {
+    DF2_OK = 0,
+    DF2_ERR_INVALID_ARG = 1, /* null pointer, bad dimension, misalignment                    */
+    DF2_ERR_UNSUPPORTED = 2, /* valid request outside the implemented limits                 */
+    DF2_ERR_WORKSPACE = 3,   /* workspace pointer null/misaligned or smaller than required   */
+    DF2_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed                         */
+    DF2_ERR_TIMEOUT = 5      /* a device-side pipeline wait gave up (see device status)      */
+} df2_status;
+
+/* Problem dimensions: B sequences x T draft positions, hidden size H, vocabulary V,
+ * candidates per position k, selector rank D. */
+typedef struct df2_dims {
+    int32_t B, T, H, V, k, D;
+} df2_dims;
+
+/* Bytes of device workspace the calls below need for `dims` (0 if dims are invalid).
+ * The first 256 bytes hold the sticky device status word: zero them once before the
+ * first call (dflash2_workspace_init).  Independent of the device. */
+DF2_API size_t dflash2_workspace_bytes(const df2_dims *dims);
+
+/* Zeroes the device status word at the start of `workspace` (cudaMemsetAsync on stream). */
+DF2_API df2_status dflash2_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The whole selector head (LM head + top-k, gate, lattice, walk) for B*T rows.
+ *   hidden   bf16 [B*T, H]   drafter hidden state of each draft position
+ *   W_vocab  bf16 [V, H]     LM-head / output-embedding rows
+ *   W_sel    bf16 [D, H]     selector projection (the context gate)
+ *   pred_cb  bf16 [V, D]     predecessor codebook A
+ *   succ_cb  bf16 [V, D]     successor codebook B
+ *   anchor   int32 [B]       last verified token of each sequence
+ * outputs:
+ *   lattice  float [B*T, k + k*k]   packed rows (layout above)
+ *   draft_ids int32 [B, T]          the greedy walk's tokens
+ *   topk_ids int32 [B*T, k], topk_logits float [B*T, k], gate float [B*T, D]:
+ *            optional copies of the candidates (sorted by logit desc, id asc), their
+ *            logits (the unary scores) and the gate; NULL to skip.
+ * The full float32 logits never reach global memory: each CTA of the tensor-core
+ * LM head keeps a per-row top-k of its vocabulary slice in registers.
+ */
+DF2_API df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *W_vocab, const void *W_sel,
+                          const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,
+                          int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate,
+                          void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Same path from given float32 logits [B*T, V] instead of the LM head: the top-k,
+ * lattice and walk see exactly these logits (the unary score of a candidate is its
+ * given logit), so the candidates and draft can be compared bit for bit.
+ */
+DF2_API df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits, const void *hidden,
+                                      const void *W_sel, const void *pred_cb, const void *succ_cb,
+                                      const int32_t *anchor, float *lattice, int32_t *draft_ids,
+                                      int32_t *topk_ids, float *topk_logits, float *gate, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/* ---- single steps of the path (same kernels as above), for stage-by-stage checks ---- */
+
+/* LM head alone: logits float [B*T, V] = hidden . W_vocab^T with float32 accumulation
+ * (tensor cores, same main loop as dflash2_select; this variant stores the tile instead
+ * of reducing it to a top-k).  dims.k and dims.D are validated but unused. */
+DF2_API df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidden, const void *W_vocab, float *logits,
+                                  void *workspace, size_t workspace_bytes, void *stream);
+
+/* Top-k of given float32 logits [B*T, V]: topk_ids int32 [B*T, k], topk_logits float [B*T, k],
+ * ordered by (logit desc, id asc).  "DFlash2 Lands in llama.cpp", candidates = top_k(logits). */
+DF2_API df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk_ids, float *topk_logits,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Gate alone: gate float [B*T, D] = hidden . W_sel^T, float32 accumulation on tensor cores. */
+DF2_API df2_status dflash2_gate(const df2_dims *dims, const void *hidden, const void *W_sel, float *gate, void *workspace,
+                        size_t workspace_bytes, void *stream);
+
+/* Lattice alone, from candidates, their unary scores and the gate: writes the packed rows. */
+DF2_API df2_status dflash2_lattice(const df2_dims *dims, const int32_t *topk_ids, const float *topk_logits,
+                           const float *gate, const void *pred_cb, const void *succ_cb, const int32_t *anchor,
+                           float *lattice, void *stream);
+
+/* Walk alone over packed rows: one warp per sequence; ties go to the lowest candidate index. */
+DF2_API df2_status dflash2_walk(const df2_dims *dims, const float *lattice, int32_t *draft_ids, void *stream);
+
+/* Synchronises `stream`, reads and clears the sticky device status word in `workspace`.
+ * Returns DF2_ERR_TIMEOUT if a pipeline wait inside any kernel gave up since the last
+ * check (the kernel then skipped its remaining work and its outputs are invalid). */
+DF2_API df2_status dflash2_check_device_status(void *workspace, size_t workspace_bytes, void *stream);
+
+/* Timing hook: on this host thread, every following dflash2_select /
+ * dflash2_select_from_logits call records `begin` on its stream just before the
+ * LM-head (or logits top-k) launch and `end` just after it, so the caller can read
+ * that kernel's duration with cudaEventElapsedTime.  Both are cudaEvent_t handles
+ * created by the caller; pass NULL, NULL to stop.  Nothing is recorded otherwise. */
+DF2_API df2_status dflash2_profile_events(void *begin, void *end);
+
+/* Static description of a status code. */
+DF2_API const char *dflash2_status_string(df2_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+DF2_API int32_t dflash2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

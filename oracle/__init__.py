@@ -65,10 +65,17 @@ def _load():
         lib.oracle_gate.argtypes = [p, p, i64, i64, i64, p]
         lib.oracle_lattice.argtypes = [i64, i64, i32, i64, i64, p, p, p, p, p, p, p, p]
         lib.oracle_walk.argtypes = [i64, i64, i32, p, p, p]
-        for f in (lib.oracle_logits, lib.oracle_topk, lib.oracle_gate, lib.oracle_lattice, lib.oracle_walk):
+        lib.oracle_threads.argtypes = []
+        for f in (lib.oracle_logits, lib.oracle_topk, lib.oracle_gate, lib.oracle_lattice, lib.oracle_walk,
+                  lib.oracle_threads):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's loops use."""
+    return int(_load().oracle_threads())
 
 
 def _ptr(a):

@@ -1,0 +1,337 @@
+// api.cu -- the C ABI declared in include/dflash2.h: argument checks, workspace
+// carving and the launch sequence of the selector head.  No allocation, no sync
+// (except dflash2_check_device_status).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "dflash2.h"
+#include "internal.h"
+
+namespace df2 {
+
+int device_sm_count()
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+df2_status check_dims(const df2_dims *d)
+{
+    if (!d)
+        return DF2_ERR_INVALID_ARG;
+    if (d->B < 1 || d->T < 1 || d->H < 1 || d->V < 1 || d->k < 1 || d->D < 1)
+        return DF2_ERR_INVALID_ARG;
+    if (d->k > d->V)
+        return DF2_ERR_INVALID_ARG;
+    if (d->k > 32 || d->V >= (1 << 24) || d->H < 8 || d->H % 8 != 0 || d->D < 8 || d->D % 8 != 0 ||
+        d->D > 1024 || static_cast<long long>(d->B) * d->T > (1LL << 20))
+        return DF2_ERR_UNSUPPORTED;
+    return DF2_OK;
+}
+
+struct Workspace {
+    uint32_t *status;
+    float *pval;
+    int32_t *pid;
+    int32_t *topk_ids;
+    float *topk_vals;
+    float *gate;
+    size_t bytes;
+};
+
+// Layout (each part 256-byte aligned): status word | partial values | partial ids |
+// top-k ids | top-k values | gate.
+Workspace carve(const df2_dims &d, void *base)
+{
+    const size_t R = static_cast<size_t>(d.B) * d.T;
+    const size_t kp = static_cast<size_t>(kp_for(d.k));
+    uint8_t *p = static_cast<uint8_t *>(base);
+    Workspace w{};
+    size_t off = 0;
+    w.status = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
+    off += kAlign;
+    w.pval = reinterpret_cast<float *>(p ? p + off : nullptr);
+    off += round_up(R * kMaxSplits * kp * sizeof(float));
+    w.pid = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
+    off += round_up(R * kMaxSplits * kp * sizeof(int32_t));
+    w.topk_ids = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
+    off += round_up(R * d.k * sizeof(int32_t));
+    w.topk_vals = reinterpret_cast<float *>(p ? p + off : nullptr);
+    off += round_up(R * d.k * sizeof(float));
+    w.gate = reinterpret_cast<float *>(p ? p + off : nullptr);
+    off += round_up(R * d.D * sizeof(float));
+    w.bytes = off;
+    return w;
+}
+
+df2_status check_workspace(const df2_dims &d, void *ws, size_t bytes)
+{
+    if (!ws || !aligned(ws, kAlign))
+        return DF2_ERR_WORKSPACE;
+    if (bytes < carve(d, nullptr).bytes)
+        return DF2_ERR_WORKSPACE;
+    return DF2_OK;
+}
+
+df2_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DF2_OK : DF2_ERR_CUDA; }
+
+// Events recorded around the top-k producing launch (dflash2_profile_events).
+thread_local cudaEvent_t t_profile_begin = nullptr;
+thread_local cudaEvent_t t_profile_end = nullptr;
+
+cudaError_t profile_mark(cudaEvent_t ev, cudaStream_t st) { return ev ? cudaEventRecord(ev, st) : cudaSuccess; }
+
+#define DF2_TRY(expr)                        \
+    do {                                     \
+        const df2_status _s = (expr);        \
+        if (_s != DF2_OK)                    \
+            return _s;                       \
+    } while (0)
+
+#define DF2_CUDA(expr) DF2_TRY(from_cuda(expr))
+
+// Shared tail of both select paths: lattice then walk.
+df2_status lattice_and_walk(const df2_dims &d, const int32_t *ids, const float *vals, const float *gate,
+                            const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,
+                            int32_t *draft_ids, cudaStream_t st)
+{
+    DF2_CUDA(launch_lattice(d.B, d.T, d.k, d.V, d.D, ids, vals, gate, static_cast<const uint16_t *>(pred_cb),
+                            static_cast<const uint16_t *>(succ_cb), anchor, lattice, st));
+    DF2_CUDA(launch_walk(d.B, d.T, d.k, lattice, draft_ids, st));
+    return DF2_OK;
+}
+
+df2_status check_tail_pointers(const void *W_sel, const void *pred_cb, const void *succ_cb, const int32_t *anchor,
+                               const float *lattice, const int32_t *draft_ids, const int32_t *topk_ids,
+                               const float *topk_logits, const float *gate)
+{
+    if (!W_sel || !pred_cb || !succ_cb || !anchor || !lattice || !draft_ids)
+        return DF2_ERR_INVALID_ARG;
+    if (!aligned(W_sel, 16) || !aligned(pred_cb, 16) || !aligned(succ_cb, 16) || !aligned(anchor, 4) ||
+        !aligned(lattice, 4) || !aligned(draft_ids, 4))
+        return DF2_ERR_INVALID_ARG;
+    if ((topk_ids && !aligned(topk_ids, 4)) || (topk_logits && !aligned(topk_logits, 4)) ||
+        (gate && !aligned(gate, 16)))
+        return DF2_ERR_INVALID_ARG;
+    return DF2_OK;
+}
+
+}  // namespace
+}  // namespace df2
+
+using namespace df2;
+
+extern "C" {
+
+size_t dflash2_workspace_bytes(const df2_dims *dims)
+{
+    if (check_dims(dims) != DF2_OK)
+        return 0;
+    return carve(*dims, nullptr).bytes;
+}
+
+df2_status dflash2_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < kAlign)
+        return DF2_ERR_WORKSPACE;
+    return from_cuda(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
+}
+
+df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *W_vocab, const void *W_sel,
+                          const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,
+                          int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate,
+                          void *workspace, size_t workspace_bytes, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!hidden || !W_vocab || !aligned(hidden, 16) || !aligned(W_vocab, 16))
+        return DF2_ERR_INVALID_ARG;
+    DF2_TRY(check_tail_pointers(W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, gate));
+    DF2_TRY(check_workspace(d, workspace, workspace_bytes));
+    cudaGetLastError();  // clear a stale error so the status reflects this call
+    const Workspace w = carve(d, workspace);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int R = d.B * d.T;
+    const int kp = kp_for(d.k);
+    int32_t *ids = topk_ids ? topk_ids : w.topk_ids;
+    float *vals = topk_logits ? topk_logits : w.topk_vals;
+    float *g = gate ? gate : w.gate;
+    int n_split = 0;
+    DF2_CUDA(profile_mark(t_profile_begin, st));
+    DF2_CUDA(launch_gemm_topk(hidden, W_vocab, R, d.H, d.V, kp, w.pval, w.pid, &n_split, w.status, st));
+    DF2_CUDA(profile_mark(t_profile_end, st));
+    DF2_CUDA(launch_gemm_store(hidden, W_sel, R, d.H, d.D, g, d.D, w.status, st));
+    DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, ids, vals, st));
+    return lattice_and_walk(d, ids, vals, g, pred_cb, succ_cb, anchor, lattice, draft_ids, st);
+}
+
+df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits, const void *hidden,
+                                      const void *W_sel, const void *pred_cb, const void *succ_cb,
+                                      const int32_t *anchor, float *lattice, int32_t *draft_ids,
+                                      int32_t *topk_ids, float *topk_logits, float *gate, void *workspace,
+                                      size_t workspace_bytes, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!logits || !hidden || !aligned(logits, 16) || !aligned(hidden, 16))
+        return DF2_ERR_INVALID_ARG;
+    DF2_TRY(check_tail_pointers(W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, gate));
+    DF2_TRY(check_workspace(d, workspace, workspace_bytes));
+    cudaGetLastError();
+    const Workspace w = carve(d, workspace);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int R = d.B * d.T;
+    const int kp = kp_for(d.k);
+    int32_t *ids = topk_ids ? topk_ids : w.topk_ids;
+    float *vals = topk_logits ? topk_logits : w.topk_vals;
+    float *g = gate ? gate : w.gate;
+    int n_split = 0;
+    DF2_CUDA(profile_mark(t_profile_begin, st));
+    DF2_CUDA(launch_logits_topk_partial(logits, R, d.V, kp, w.pval, w.pid, &n_split, st));
+    DF2_CUDA(profile_mark(t_profile_end, st));
+    DF2_CUDA(launch_gemm_store(hidden, W_sel, R, d.H, d.D, g, d.D, w.status, st));
+    DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, ids, vals, st));
+    return lattice_and_walk(d, ids, vals, g, pred_cb, succ_cb, anchor, lattice, draft_ids, st);
+}
+
+df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidden, const void *W_vocab, float *logits,
+                                  void *workspace, size_t workspace_bytes, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!hidden || !W_vocab || !logits || !aligned(hidden, 16) || !aligned(W_vocab, 16) || !aligned(logits, 4))
+        return DF2_ERR_INVALID_ARG;
+    DF2_TRY(check_workspace(d, workspace, workspace_bytes));
+    cudaGetLastError();
+    const Workspace w = carve(d, workspace);
+    DF2_CUDA(launch_gemm_store(hidden, W_vocab, d.B * d.T, d.H, d.V, logits, d.V, w.status,
+                               static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
+df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk_ids, float *topk_logits,
+                        void *workspace, size_t workspace_bytes, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!logits || !topk_ids || !topk_logits || !aligned(logits, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_logits, 4))
+        return DF2_ERR_INVALID_ARG;
+    DF2_TRY(check_workspace(d, workspace, workspace_bytes));
+    cudaGetLastError();
+    const Workspace w = carve(d, workspace);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int R = d.B * d.T;
+    const int kp = kp_for(d.k);
+    int n_split = 0;
+    DF2_CUDA(launch_logits_topk_partial(logits, R, d.V, kp, w.pval, w.pid, &n_split, st));
+    DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, topk_ids, topk_logits, st));
+    return DF2_OK;
+}
+
+df2_status dflash2_gate(const df2_dims *dims, const void *hidden, const void *W_sel, float *gate, void *workspace,
+                        size_t workspace_bytes, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!hidden || !W_sel || !gate || !aligned(hidden, 16) || !aligned(W_sel, 16) || !aligned(gate, 16))
+        return DF2_ERR_INVALID_ARG;
+    DF2_TRY(check_workspace(d, workspace, workspace_bytes));
+    cudaGetLastError();
+    const Workspace w = carve(d, workspace);
+    DF2_CUDA(launch_gemm_store(hidden, W_sel, d.B * d.T, d.H, d.D, gate, d.D, w.status,
+                               static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
+df2_status dflash2_lattice(const df2_dims *dims, const int32_t *topk_ids, const float *topk_logits,
+                           const float *gate, const void *pred_cb, const void *succ_cb, const int32_t *anchor,
+                           float *lattice, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!topk_ids || !topk_logits || !gate || !pred_cb || !succ_cb || !anchor || !lattice)
+        return DF2_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(topk_logits, 4) || !aligned(gate, 16) || !aligned(pred_cb, 16) ||
+        !aligned(succ_cb, 16) || !aligned(anchor, 4) || !aligned(lattice, 4))
+        return DF2_ERR_INVALID_ARG;
+    cudaGetLastError();
+    DF2_CUDA(launch_lattice(d.B, d.T, d.k, d.V, d.D, topk_ids, topk_logits, gate,
+                            static_cast<const uint16_t *>(pred_cb), static_cast<const uint16_t *>(succ_cb), anchor,
+                            lattice, static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
+df2_status dflash2_walk(const df2_dims *dims, const float *lattice, int32_t *draft_ids, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!lattice || !draft_ids || !aligned(lattice, 4) || !aligned(draft_ids, 4))
+        return DF2_ERR_INVALID_ARG;
+    cudaGetLastError();
+    DF2_CUDA(launch_walk(d.B, d.T, d.k, lattice, draft_ids, static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
+df2_status dflash2_check_device_status(void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < kAlign)
+        return DF2_ERR_WORKSPACE;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    DF2_CUDA(cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st));
+    DF2_CUDA(cudaStreamSynchronize(st));
+    if (word != 0) {
+        DF2_CUDA(cudaMemsetAsync(workspace, 0, sizeof word, st));
+        DF2_CUDA(cudaStreamSynchronize(st));
+        return DF2_ERR_TIMEOUT;
+    }
+    return DF2_OK;
+}
+
+df2_status dflash2_profile_events(void *begin, void *end)
+{
+    if ((begin == nullptr) != (end == nullptr))
+        return DF2_ERR_INVALID_ARG;
+    t_profile_begin = static_cast<cudaEvent_t>(begin);
+    t_profile_end = static_cast<cudaEvent_t>(end);
+    return DF2_OK;
+}
+
+const char *dflash2_status_string(df2_status status)
+{
+    switch (status) {
+    case DF2_OK: return "ok";
+    case DF2_ERR_INVALID_ARG: return "invalid argument (null pointer, bad dimension or misaligned tensor)";
+    case DF2_ERR_UNSUPPORTED: return "unsupported dimensions (outside the implemented limits)";
+    case DF2_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case DF2_ERR_CUDA: return "CUDA runtime or launch error";
+    case DF2_ERR_TIMEOUT: return "a device-side pipeline wait timed out; outputs are invalid";
+    default: return "unknown status";
+    }
+}
+
+int32_t dflash2_version(void) { return 100; }
+
+}  // extern "C"

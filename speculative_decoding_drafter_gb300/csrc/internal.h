@@ -1,0 +1,46 @@
+// internal.h -- launchers shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace df2 {
+
+// Partial top-k lists hold at most this many vocabulary splits per row.
+constexpr int kMaxSplits = 256;
+
+// Capacity of the per-row candidate lists for a requested k (4, 8, 16 or 32).
+inline int kp_for(int k) { return k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32; }
+
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
+// C[R, N] = A[R, K] . B[N, K]^T on tensor cores (bf16 in, float32 accumulate), reduced
+// on the fly to per-row top-KP lists over each CTA's column slice:
+// pval/pid [R, n_split, KP] (value desc, id asc).  *n_split_out receives the split count.
+cudaError_t launch_gemm_topk(const void *A, const void *B, int R, int K, int N, int KP, float *pval, int32_t *pid,
+                             int *n_split_out, uint32_t *status, cudaStream_t stream);
+
+// Same product stored as float32: out[r * ldo + n].
+cudaError_t launch_gemm_store(const void *A, const void *B, int R, int K, int N, float *out, long long ldo,
+                              uint32_t *status, cudaStream_t stream);
+
+// Per-row partial top-KP of given float32 logits [R, V] over n_split column slices.
+cudaError_t launch_logits_topk_partial(const float *logits, int R, int V, int KP, float *pval, int32_t *pid,
+                                       int *n_split_out, cudaStream_t stream);
+
+// Merge [R, n_split, KP] partial lists into the top-k of each row (value desc, id asc).
+cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int n_split, int KP, int k,
+                              int32_t *topk_ids, float *topk_vals, cudaStream_t stream);
+
+// Packed lattice rows [B*T, k + k*k] from candidates, unary scores, gate and codebooks.
+cudaError_t launch_lattice(int B, int T, int k, int V, int D, const int32_t *topk_ids, const float *topk_vals,
+                           const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
+                           const int32_t *anchor, float *lattice, cudaStream_t stream);
+
+// Greedy walk, one warp per sequence: draft_ids [B, T].
+cudaError_t launch_walk(int B, int T, int k, const float *lattice, int32_t *draft_ids, cudaStream_t stream);
+
+}  // namespace df2

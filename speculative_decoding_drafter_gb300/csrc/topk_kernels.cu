@@ -1,0 +1,146 @@
+// topk_kernels.cu -- top-k of materialised float32 logits, and the merge of partial lists.
+//
+// "DFlash2 Lands in llama.cpp", section "What llama.cpp Actually Builds for the
+// Selector": candidates = top_k(logits); the unary scores are the gathered logits.
+// Order: value descending, then token id ascending.
+#include <algorithm>
+#include <cstdint>
+
+#include "internal.h"
+#include "topk.cuh"
+
+namespace df2 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// One CTA per (row, column slice).  Each thread keeps a register top-KP over the
+// columns it reads (in increasing id order), each warp merges its 32 lists, and
+// warp 0 merges the 8 warp lists into the slice's partial list.
+template <int KP, bool kVec4>
+__global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const float *__restrict__ logits, int V,
+                                                                       int n_split, float *__restrict__ pval,
+                                                                       int32_t *__restrict__ pid)
+{
+    const int r = blockIdx.x;
+    const int s = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const float *row = logits + static_cast<long long>(r) * V;
+    ThreadTopK<KP> top;
+    top.init();
+    if constexpr (kVec4) {
+        const int groups = V / 4;
+        const int g0 = static_cast<int>(static_cast<long long>(s) * groups / n_split);
+        const int g1 = static_cast<int>(static_cast<long long>(s + 1) * groups / n_split);
+        const float4 *row4 = reinterpret_cast<const float4 *>(row);
+        for (int g = g0 + threadIdx.x; g < g1; g += kThreads) {
+            const float4 x = __ldcs(row4 + g);
+            const float thr = top.threshold();
+            if (x.x > thr || x.y > thr || x.z > thr || x.w > thr) {
+                top.push_increasing_id(x.x, 4 * g);
+                top.push_increasing_id(x.y, 4 * g + 1);
+                top.push_increasing_id(x.z, 4 * g + 2);
+                top.push_increasing_id(x.w, 4 * g + 3);
+            }
+        }
+    } else {
+        const int e0 = static_cast<int>(static_cast<long long>(s) * V / n_split);
+        const int e1 = static_cast<int>(static_cast<long long>(s + 1) * V / n_split);
+        for (int e = e0 + threadIdx.x; e < e1; e += kThreads)
+            top.push_increasing_id(__ldcs(row + e), e);
+    }
+
+    WarpList wl;
+    wl.init();
+#pragma unroll
+    for (int j = 0; j < KP; ++j)
+        wl.offer(top.v[j], top.i[j], KP);
+
+    __shared__ float sv[kWarps][32];
+    __shared__ int si[kWarps][32];
+    sv[warp][lane] = wl.v;
+    si[warp][lane] = wl.i;
+    __syncthreads();
+    if (warp == 0) {
+        WarpList fl;
+        fl.init();
+        for (int w = 0; w < kWarps; ++w) {
+            const bool in = lane < KP;
+            fl.offer(in ? sv[w][lane] : -INFINITY, in ? si[w][lane] : INT_MAX, KP);
+        }
+        if (lane < KP) {
+            const long long base = (static_cast<long long>(r) * n_split + s) * KP;
+            pval[base + lane] = fl.v;
+            pid[base + lane] = fl.i;
+        }
+    }
+}
+
+// One warp per row: merge n_split sorted lists of KP into the row's top-k.
+__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float *__restrict__ pval,
+                                                              const int32_t *__restrict__ pid, int R, int total,
+                                                              int k, int32_t *__restrict__ ids,
+                                                              float *__restrict__ vals)
+{
+    const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= R)
+        return;
+    const long long base = static_cast<long long>(r) * total;
+    WarpList wl;
+    wl.init();
+    for (int c = 0; c < total; c += 32) {
+        const int idx = c + lane;
+        const float cv = idx < total ? pval[base + idx] : -INFINITY;
+        const int ci = idx < total ? pid[base + idx] : INT_MAX;
+        wl.offer(cv, ci, k);
+    }
+    if (lane < k) {
+        ids[static_cast<long long>(r) * k + lane] = wl.i;
+        vals[static_cast<long long>(r) * k + lane] = wl.v;
+    }
+}
+
+template <int KP>
+cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32_t *pid, int *n_split_out,
+                           cudaStream_t stream)
+{
+    // about four CTAs per SM in total, slices of at least 2048 columns
+    const int sms = device_sm_count();
+    int n_split = std::max(1, (4 * sms + R - 1) / R);
+    n_split = std::min({n_split, kMaxSplits, std::max(1, V / 2048)});
+    *n_split_out = n_split;
+    const dim3 grid(static_cast<unsigned>(R), static_cast<unsigned>(n_split));
+    const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
+    if (vec4)
+        logits_topk_partial_kernel<KP, true><<<grid, kThreads, 0, stream>>>(logits, V, n_split, pval, pid);
+    else
+        logits_topk_partial_kernel<KP, false><<<grid, kThreads, 0, stream>>>(logits, V, n_split, pval, pid);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_logits_topk_partial(const float *logits, int R, int V, int KP, float *pval, int32_t *pid,
+                                       int *n_split_out, cudaStream_t stream)
+{
+    switch (KP) {
+    case 4: return launch_partial<4>(logits, R, V, pval, pid, n_split_out, stream);
+    case 8: return launch_partial<8>(logits, R, V, pval, pid, n_split_out, stream);
+    case 16: return launch_partial<16>(logits, R, V, pval, pid, n_split_out, stream);
+    case 32: return launch_partial<32>(logits, R, V, pval, pid, n_split_out, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int n_split, int KP, int k,
+                              int32_t *topk_ids, float *topk_vals, cudaStream_t stream)
+{
+    const dim3 grid(static_cast<unsigned>((R + kWarps - 1) / kWarps));
+    topk_merge_kernel<<<grid, kThreads, 0, stream>>>(pval, pid, R, n_split * KP, k, topk_ids, topk_vals);
+    return cudaGetLastError();
+}
+
+}  // namespace df2

@@ -1,0 +1,304 @@
+"""Thin ctypes binding of libdflash2.so (the C ABI in include/dflash2.h).
+
+Functions carry the C names and only marshal arguments: torch CUDA tensors are
+checked for dtype, device, shape and contiguity, their data pointers and the
+current CUDA stream are passed through, and a non-OK status raises
+:class:`DFlash2Error`.  Every step of the selector head runs in the library's
+CUDA kernels; there is no CPU or PyTorch fallback, and a missing library is
+an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB_PATH
+
+__all__ = [
+    "DFlash2Error", "Dims", "library", "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select",
+    "dflash2_select_from_logits", "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice",
+    "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
+    "dflash2_profile_events",
+    "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = (
+    "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select", "dflash2_select_from_logits",
+    "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
+    "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
+)
+
+
+class DFlash2Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({_status_string(status)})")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("D", ctypes.c_int32)]
+
+    def __repr__(self):
+        return f"Dims(B={self.B}, T={self.T}, H={self.H}, V={self.V}, k={self.k}, D={self.D})"
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library(path: str | None = None):
+    """Load libdflash2.so (built by ``__graft_entry__.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = path or LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is not built; run speculative_decoding_drafter_gb300.build.build() "
+                                   "(nvcc, sm_103a) first -- there is no fallback path")
+            lib = ctypes.CDLL(path)
+            P, S, I = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+            D = ctypes.POINTER(Dims)
+            sig = {
+                "dflash2_workspace_bytes": (S, [D]),
+                "dflash2_workspace_init": (I, [P, S, P]),
+                "dflash2_select": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
+                "dflash2_select_from_logits": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
+                "dflash2_lm_head_logits": (I, [D, P, P, P, P, S, P]),
+                "dflash2_topk": (I, [D, P, P, P, P, S, P]),
+                "dflash2_gate": (I, [D, P, P, P, P, S, P]),
+                "dflash2_lattice": (I, [D, P, P, P, P, P, P, P, P]),
+                "dflash2_walk": (I, [D, P, P, P]),
+                "dflash2_check_device_status": (I, [P, S, P]),
+                "dflash2_status_string": (ctypes.c_char_p, [I]),
+                "dflash2_version": (ctypes.c_int32, []),
+                "dflash2_profile_events": (I, [P, P]),
+            }
+            for name, (res, args) in sig.items():
+                f = getattr(lib, name)
+                f.restype, f.argtypes = res, args
+            _lib = lib
+        return _lib
+
+
+def _status_string(status: int) -> str:
+    try:
+        return library().dflash2_status_string(status).decode()
+    except Exception:  # pragma: no cover - only when the library itself is missing
+        return "unknown"
+
+
+def dflash2_status_string(status: int) -> str:
+    return library().dflash2_status_string(int(status)).decode()
+
+
+def dflash2_version() -> int:
+    return int(library().dflash2_version())
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise DFlash2Error(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t, dtype, shape, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def make_dims(B, T, H, V, k, D) -> Dims:
+    return Dims(int(B), int(T), int(H), int(V), int(k), int(D))
+
+
+def dflash2_workspace_bytes(dims: Dims) -> int:
+    return int(library().dflash2_workspace_bytes(ctypes.byref(dims)))
+
+
+def dflash2_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    _check(library().dflash2_workspace_init(workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "dflash2_workspace_init")
+
+
+class Workspace:
+    """Device scratch for one problem size (uint8 tensor, 256-byte aligned, status word zeroed)."""
+
+    def __init__(self, dims: Dims, device=None):
+        n = dflash2_workspace_bytes(dims)
+        if n == 0:
+            raise ValueError(f"invalid or unsupported dims {dims}")
+        self.dims = dims
+        self.tensor = torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.tensor.data_ptr()) % 256
+        self.view = self.tensor[off:off + n]
+        self.nbytes = n
+
+    @property
+    def ptr(self) -> int:
+        return self.view.data_ptr()
+
+
+def _workspace(ws, dims, device):
+    if ws is None:
+        return Workspace(dims, device)
+    if ws.nbytes < dflash2_workspace_bytes(dims):
+        raise ValueError("workspace too small for these dims")
+    return ws
+
+
+def _dims_of(hidden, W_vocab_or_none, W_sel, pred_cb, k, T, V=None):
+    R, H = hidden.shape
+    if R % T:
+        raise ValueError(f"hidden has {R} rows, not a multiple of T={T}")
+    V = V if V is not None else W_vocab_or_none.shape[0]
+    D = W_sel.shape[0]
+    return make_dims(R // T, T, H, V, k, D)
+
+
+def dflash2_select(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, lattice=None,
+                   draft_ids=None, topk_ids=None, topk_logits=None, gate=None, workspace=None, stream=None):
+    """Whole selector head on the GPU. Returns (lattice [B*T, k+k*k] float32, draft_ids [B, T] int32)."""
+    d = _dims_of(hidden, W_vocab, W_sel, pred_cb, k, T)
+    dev = hidden.device
+    R = d.B * d.T
+    lattice = lattice if lattice is not None else torch.empty((R, k + k * k), dtype=torch.float32, device=dev)
+    draft_ids = draft_ids if draft_ids is not None else torch.empty((d.B, T), dtype=torch.int32, device=dev)
+    ws = _workspace(workspace, d, dev)
+    bf = torch.bfloat16
+    st = library().dflash2_select(
+        ctypes.byref(d), _ptr(hidden, bf, (R, d.H), "hidden"), _ptr(W_vocab, bf, (d.V, d.H), "W_vocab"),
+        _ptr(W_sel, bf, (d.D, d.H), "W_sel"), _ptr(pred_cb, bf, (d.V, d.D), "pred_cb"),
+        _ptr(succ_cb, bf, (d.V, d.D), "succ_cb"), _ptr(anchor, torch.int32, (d.B,), "anchor"),
+        _ptr(lattice, torch.float32, (R, k + k * k), "lattice"), _ptr(draft_ids, torch.int32, (d.B, T), "draft_ids"),
+        _ptr(topk_ids, torch.int32, (R, k), "topk_ids"), _ptr(topk_logits, torch.float32, (R, k), "topk_logits"),
+        _ptr(gate, torch.float32, (R, d.D), "gate"), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "dflash2_select")
+    return lattice, draft_ids
+
+
+def dflash2_select_from_logits(logits, hidden, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, lattice=None,
+                               draft_ids=None, topk_ids=None, topk_logits=None, gate=None, workspace=None,
+                               stream=None):
+    """Selector head from given float32 logits [B*T, V]. Returns (lattice, draft_ids)."""
+    d = _dims_of(hidden, None, W_sel, pred_cb, k, T, V=logits.shape[1])
+    dev = hidden.device
+    R = d.B * d.T
+    lattice = lattice if lattice is not None else torch.empty((R, k + k * k), dtype=torch.float32, device=dev)
+    draft_ids = draft_ids if draft_ids is not None else torch.empty((d.B, T), dtype=torch.int32, device=dev)
+    ws = _workspace(workspace, d, dev)
+    bf = torch.bfloat16
+    st = library().dflash2_select_from_logits(
+        ctypes.byref(d), _ptr(logits, torch.float32, (R, d.V), "logits"), _ptr(hidden, bf, (R, d.H), "hidden"),
+        _ptr(W_sel, bf, (d.D, d.H), "W_sel"), _ptr(pred_cb, bf, (d.V, d.D), "pred_cb"),
+        _ptr(succ_cb, bf, (d.V, d.D), "succ_cb"), _ptr(anchor, torch.int32, (d.B,), "anchor"),
+        _ptr(lattice, torch.float32, (R, k + k * k), "lattice"), _ptr(draft_ids, torch.int32, (d.B, T), "draft_ids"),
+        _ptr(topk_ids, torch.int32, (R, k), "topk_ids"), _ptr(topk_logits, torch.float32, (R, k), "topk_logits"),
+        _ptr(gate, torch.float32, (R, d.D), "gate"), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "dflash2_select_from_logits")
+    return lattice, draft_ids
+
+
+def dflash2_lm_head_logits(hidden, W_vocab, *, out=None, workspace=None, stream=None):
+    """float32 logits [R, V] from the tensor-core LM head (stage check / standalone use)."""
+    R, H = hidden.shape
+    V = W_vocab.shape[0]
+    d = make_dims(R, 1, H, V, 1, 8)
+    out = out if out is not None else torch.empty((R, V), dtype=torch.float32, device=hidden.device)
+    ws = _workspace(workspace, d, hidden.device)
+    bf = torch.bfloat16
+    st = library().dflash2_lm_head_logits(ctypes.byref(d), _ptr(hidden, bf, (R, H), "hidden"),
+                                          _ptr(W_vocab, bf, (V, H), "W_vocab"),
+                                          _ptr(out, torch.float32, (R, V), "logits"), ws.ptr, ws.nbytes,
+                                          _stream(stream))
+    _check(st, "dflash2_lm_head_logits")
+    return out
+
+
+def dflash2_topk(logits, k: int, *, ids=None, vals=None, workspace=None, stream=None):
+    """Top-k of float32 logits [R, V] by (value desc, id asc). Returns (ids int32 [R,k], vals float32 [R,k])."""
+    R, V = logits.shape
+    d = make_dims(R, 1, 8, V, k, 8)
+    ids = ids if ids is not None else torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    vals = vals if vals is not None else torch.empty((R, k), dtype=torch.float32, device=logits.device)
+    ws = _workspace(workspace, d, logits.device)
+    st = library().dflash2_topk(ctypes.byref(d), _ptr(logits, torch.float32, (R, V), "logits"),
+                                _ptr(ids, torch.int32, (R, k), "topk_ids"),
+                                _ptr(vals, torch.float32, (R, k), "topk_logits"), ws.ptr, ws.nbytes,
+                                _stream(stream))
+    _check(st, "dflash2_topk")
+    return ids, vals
+
+
+def dflash2_gate(hidden, W_sel, *, out=None, workspace=None, stream=None):
+    """Gate float32 [R, D] = hidden . W_sel^T on tensor cores."""
+    R, H = hidden.shape
+    D = W_sel.shape[0]
+    d = make_dims(R, 1, H, max(1, D), 1, D)
+    out = out if out is not None else torch.empty((R, D), dtype=torch.float32, device=hidden.device)
+    ws = _workspace(workspace, d, hidden.device)
+    bf = torch.bfloat16
+    st = library().dflash2_gate(ctypes.byref(d), _ptr(hidden, bf, (R, H), "hidden"), _ptr(W_sel, bf, (D, H), "W_sel"),
+                                _ptr(out, torch.float32, (R, D), "gate"), ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "dflash2_gate")
+    return out
+
+
+def dflash2_lattice(topk_ids, topk_logits, gate, pred_cb, succ_cb, anchor, T: int, *, out=None, stream=None):
+    """Packed lattice [B*T, k+k*k] from candidates, unary scores and the gate."""
+    R, k = topk_ids.shape
+    V, D = pred_cb.shape
+    B = anchor.shape[0]
+    if R != B * T:
+        raise ValueError("topk_ids rows must equal B*T")
+    d = make_dims(B, T, 8, V, k, D)
+    out = out if out is not None else torch.empty((R, k + k * k), dtype=torch.float32, device=topk_ids.device)
+    bf = torch.bfloat16
+    st = library().dflash2_lattice(ctypes.byref(d), _ptr(topk_ids, torch.int32, (R, k), "topk_ids"),
+                                   _ptr(topk_logits, torch.float32, (R, k), "topk_logits"),
+                                   _ptr(gate, torch.float32, (R, D), "gate"), _ptr(pred_cb, bf, (V, D), "pred_cb"),
+                                   _ptr(succ_cb, bf, (V, D), "succ_cb"), _ptr(anchor, torch.int32, (B,), "anchor"),
+                                   _ptr(out, torch.float32, (R, k + k * k), "lattice"), _stream(stream))
+    _check(st, "dflash2_lattice")
+    return out
+
+
+def dflash2_walk(lattice, B: int, T: int, k: int, *, out=None, stream=None):
+    """Greedy walk over packed rows: draft ids int32 [B, T]."""
+    d = make_dims(B, T, 8, max(k, 1), k, 8)
+    out = out if out is not None else torch.empty((B, T), dtype=torch.int32, device=lattice.device)
+    st = library().dflash2_walk(ctypes.byref(d), _ptr(lattice, torch.float32, (B * T, k + k * k), "lattice"),
+                                _ptr(out, torch.int32, (B, T), "draft_ids"), _stream(stream))
+    _check(st, "dflash2_walk")
+    return out
+
+
+def dflash2_check_device_status(workspace: Workspace, stream=None) -> None:
+    """Synchronises the stream; raises DFlash2Error(DF2_ERR_TIMEOUT) if a kernel wait gave up."""
+    _check(library().dflash2_check_device_status(workspace.ptr, workspace.nbytes, _stream(stream)),
+           "dflash2_check_device_status")
+
+
+def dflash2_profile_events(begin=None, end=None) -> None:
+    """Record torch.cuda.Event pairs around the LM-head launch of following select calls (None, None stops)."""
+    b = None if begin is None else begin.cuda_event
+    e = None if end is None else end.cuda_event
+    _check(library().dflash2_profile_events(b, e), "dflash2_profile_events")

@@ -1,0 +1,272 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on a GB300.
+
+Every config of the selector head runs at its full size through
+dflash2_select, in the same launch configuration the benchmark times; the
+oracle recomputes a sample of whole sequences (the lattice is block-local, so
+a sequence's outputs depend only on its own rows).  Stage tests cover each
+kernel alone on ragged shapes that span several tiles and tails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_rules import (check_fused_candidates, check_sorted_lists, compare_lattice_and_draft, dev, dev_bf16,
+                          host, row_tol)
+from speculative_decoding_drafter_gb300 import dflash2 as df
+from speculative_decoding_drafter_gb300.synth import CONFIGS, SelectorConfig, bf16_bits_to_f32, f32_to_bf16_bits, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+U32 = 2.0 ** -24
+
+
+def sampled_sequences(x):
+    cfg = x["cfg"]
+    if cfg.B <= 2:
+        return list(range(cfg.B))
+    plant_rows = x["plant"].get("rows", [])
+    seqs = sorted({r // cfg.T for r in plant_rows})[:2]
+    for b in (0, cfg.B - 1):
+        if len(seqs) >= 3:
+            break
+        if b not in seqs:
+            seqs.append(b)
+    return sorted(seqs)
+
+
+def rows_of(seqs, T):
+    return np.concatenate([np.arange(b * T, (b + 1) * T) for b in seqs])
+
+
+@pytest.fixture(scope="module", params=list(CONFIGS))
+def case(request):
+    cfg = CONFIGS[request.param]
+    x = make_inputs(cfg, 0)
+    seqs = sampled_sequences(x)
+    rows = rows_of(seqs, cfg.T)
+    d = {n: dev_bf16(x[n]) for n in ("hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb")}
+    d["anchor"] = dev(x["anchor"])
+    R, k = cfg.R, cfg.k
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    gate = torch.empty((R, cfg.D), dtype=torch.float32, device="cuda")
+    ws = df.Workspace(df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, k, cfg.D))
+    lat, draft = df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], d["anchor"], k,
+                                   cfg.T, topk_ids=ids, topk_logits=vals, gate=gate, workspace=ws)
+    torch.cuda.synchronize()
+    df.dflash2_check_device_status(ws)
+    ora = oracle.select(x["hidden"][rows], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"][seqs], k,
+                        cfg.T)
+    out = {"cfg": cfg, "x": x, "d": d, "seqs": seqs, "rows": rows, "ws": ws, "ora": ora,
+           "lat": host(lat), "draft": host(draft), "ids": host(ids), "vals": host(vals), "gate": host(gate)}
+    yield out
+    del d, out
+    torch.cuda.empty_cache()
+
+
+def test_select_candidates_match_oracle(case):
+    ora, rows = case["ora"], case["rows"]
+    tol = row_tol(ora["logits"])
+    swaps = check_fused_candidates(case["ids"][rows], case["vals"][rows], ora["logits"], ora["topk_ids"],
+                                   ora["topk_vals"], tol)
+    assert swaps <= max(1, len(rows) // 50), f"{swaps} near-tie swaps in {len(rows)} rows"
+    # the packed ids are the candidate lists, as exact floats
+    k = case["cfg"].k
+    assert np.array_equal(case["lat"][:, :k], case["ids"].astype(np.float32))
+
+
+def test_select_lattice_and_draft_match_oracle(case):
+    cfg, ora, rows, seqs = case["cfg"], case["ora"], case["rows"], case["seqs"]
+    tol = row_tol(ora["logits"])
+    compared, low = compare_lattice_and_draft(case["lat"][rows], case["draft"][seqs], ora, cfg.T, cfg.k, tol)
+    assert compared + low >= 1
+    assert compared >= (len(seqs) * cfg.T) // 2, f"only {compared} draft steps were comparable"
+
+
+def test_select_gate_matches_oracle(case):
+    cfg, x, rows = case["cfg"], case["x"], case["rows"]
+    h = bf16_bits_to_f32(x["hidden"][rows]).astype(np.float64)
+    w = bf16_bits_to_f32(x["W_sel"]).astype(np.float64)
+    bound = 2 * cfg.H * U32 * (np.abs(h) @ np.abs(w).T) + 1e-30
+    err = np.abs(case["gate"][rows].astype(np.float64) - case["ora"]["gate"])
+    assert np.all(err <= bound), f"gate error {err.max()} exceeds the float32 summation bound"
+
+
+def test_select_from_oracle_logits_is_exact(case):
+    """Given identical float32 logits: ids and unary bit-exact, lattice tight, draft exact."""
+    cfg, x, ora, rows, seqs = case["cfg"], case["x"], case["ora"], case["rows"], case["seqs"]
+    d, k = case["d"], cfg.k
+    Rs = len(rows)
+    ids = torch.empty((Rs, k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((Rs, k), dtype=torch.float32, device="cuda")
+    lat, draft = df.dflash2_select_from_logits(dev(ora["logits"]), d["hidden"][torch.from_numpy(rows).cuda()].contiguous(),
+                                               d["W_sel"], d["pred_cb"], d["succ_cb"], dev(x["anchor"][seqs]), k, cfg.T,
+                                               topk_ids=ids, topk_logits=vals)
+    torch.cuda.synchronize()
+    assert np.array_equal(host(ids), ora["topk_ids"])
+    assert np.array_equal(host(vals).view(np.uint32), ora["topk_vals"].view(np.uint32))
+    tight = 2e-5 * (1.0 + np.abs(ora["logits"]).max(axis=1))
+    compared, low = compare_lattice_and_draft(host(lat), host(draft), ora, cfg.T, k, row_tol(ora["logits"]),
+                                              margin_floor=tight)
+    assert low == 0, f"{low} walk steps with margin below {tight.min():.2e}"
+    assert compared == len(seqs) * cfg.T
+
+
+def test_select_is_deterministic(case):
+    cfg, d = case["cfg"], case["d"]
+    lat, draft = df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], d["anchor"],
+                                   cfg.k, cfg.T, workspace=case["ws"])
+    torch.cuda.synchronize()
+    assert np.array_equal(host(lat).view(np.uint32), case["lat"].view(np.uint32))
+    assert np.array_equal(host(draft), case["draft"])
+
+
+def test_duplicate_logits_break_ties_by_lower_id(case):
+    if case["cfg"].plant != "dup_logits":
+        pytest.skip("config has no duplicate logits")
+    ids, vals = case["ids"], case["vals"]
+    seen = 0
+    for r, v, u in case["x"]["plant"]["pairs"]:
+        row = ids[r].tolist()
+        if v in row and u in row:
+            a, b = row.index(v), row.index(u)
+            assert vals[r, a] == vals[r, b], "duplicate vocabulary rows gave different logits"
+            lo, hi = (a, b) if v < u else (b, a)
+            assert lo < hi, f"row {r}: higher id {max(u, v)} ranked before {min(u, v)}"
+            seen += 1
+    assert seen >= len(case["x"]["plant"]["pairs"]) // 2
+
+
+# ---------------------------------------------------------------- stage tests on ragged shapes
+
+
+def rand_bf16(rng, shape, std=1.0):
+    return f32_to_bf16_bits((rng.standard_normal(shape) * std).astype(np.float32))
+
+
+@pytest.mark.parametrize("R,H,V", [(8, 256, 4096), (37, 200, 1013), (300, 136, 2000), (1, 64, 16), (130, 4096, 600)])
+def test_lm_head_logits_stage(R, H, V):
+    rng = np.random.default_rng(R * 7 + V)
+    h = rand_bf16(rng, (R, H))
+    w = rand_bf16(rng, (V, H), 1 / np.sqrt(H))
+    got = host(df.dflash2_lm_head_logits(dev_bf16(h), dev_bf16(w)))
+    ora = oracle.logits(h, w)
+    bound = 2 * H * U32 * (np.abs(bf16_bits_to_f32(h)).astype(np.float64) @ np.abs(bf16_bits_to_f32(w)).T.astype(np.float64))
+    assert np.all(np.abs(got.astype(np.float64) - ora) <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("R,V,k", [(3, 50, 5), (16, 151936, 8), (7, 4099, 32), (2, 40, 32), (5, 3000, 1), (64, 262144, 16)])
+def test_topk_stage_is_exact(R, V, k):
+    rng = np.random.default_rng(V + k)
+    lg = rng.standard_normal((R, V)).astype(np.float32)
+    lg[:, 7 % V] = lg[:, 3 % V]  # duplicates
+    lg[0, : min(V, 20)] = 4.0  # a run of equal maxima
+    if R > 1:
+        lg[1, 5 % V], lg[1, 9 % V] = np.float32(-0.0), np.float32(0.0)
+        lg[1] = np.where(np.arange(V) % 2 == 0, -np.abs(lg[1]), lg[1])
+    ids, vals = df.dflash2_topk(dev(lg), k)
+    o_ids, o_vals = oracle.topk(lg, k)
+    assert np.array_equal(host(ids), o_ids)
+    assert np.array_equal(host(vals).view(np.uint32), o_vals.view(np.uint32))
+
+
+@pytest.mark.parametrize("R,H,D", [(8, 256, 64), (33, 200, 24), (300, 4096, 256), (1024, 512, 512)])
+def test_gate_stage(R, H, D):
+    rng = np.random.default_rng(R + H + D)
+    h = rand_bf16(rng, (R, H))
+    w = rand_bf16(rng, (D, H), 1 / np.sqrt(H))
+    got = host(df.dflash2_gate(dev_bf16(h), dev_bf16(w))).astype(np.float64)
+    ora = oracle.gate(h, w)
+    bound = 2 * H * U32 * (np.abs(bf16_bits_to_f32(h)).astype(np.float64) @ np.abs(bf16_bits_to_f32(w)).T.astype(np.float64))
+    assert np.all(np.abs(got - ora) <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("B,T,k,V,D", [(2, 5, 4, 100, 16), (3, 4, 16, 500, 512), (1, 1, 1, 10, 8), (2, 3, 32, 64, 1024)])
+def test_lattice_stage(B, T, k, V, D):
+    rng = np.random.default_rng(B * T * k + D)
+    cand = np.stack([rng.choice(V, size=k, replace=False) for _ in range(B * T)]).astype(np.int32)
+    U = rng.standard_normal((B * T, k)).astype(np.float32)
+    g = rng.standard_normal((B * T, D)).astype(np.float32)
+    pred = rand_bf16(rng, (V, D), 0.1)
+    succ = rand_bf16(rng, (V, D), 0.1)
+    anchor = rng.integers(0, V, B).astype(np.int32)
+    got = host(df.dflash2_lattice(dev(cand), dev(U), dev(g), dev_bf16(pred), dev_bf16(succ), dev(anchor), T))
+    want = oracle.lattice(cand, U, g.astype(np.float64), pred, succ, anchor, T)
+    assert np.array_equal(got[:, :k], want[:, :k])
+    # float32 summation bound: 2 (D + 2) u (|U| + sum_d |A g B|), u = 2^-24
+    pa, sa = np.abs(bf16_bits_to_f32(pred)).astype(np.float64), np.abs(bf16_bits_to_f32(succ)).astype(np.float64)
+    bound = np.zeros((B * T, k, k))
+    for r in range(B * T):
+        t = r % T
+        prev = np.full(k, anchor[r // T]) if t == 0 else cand[r - 1]
+        absum = (pa[prev] * np.abs(g[r].astype(np.float64))) @ sa[cand[r]].T
+        bound[r] = 2 * (D + 2) * U32 * (np.abs(U[r]).astype(np.float64)[None, :] + absum)
+    err = np.abs(got[:, k:].astype(np.float64) - want[:, k:].astype(np.float64)).reshape(B * T, k, k)
+    assert np.all(err <= bound + 1e-30)
+
+
+@pytest.mark.parametrize("B,T,k", [(1, 16, 8), (5, 7, 16), (3, 4, 1), (2, 9, 32)])
+def test_walk_stage_is_exact(B, T, k):
+    rng = np.random.default_rng(B + T + k)
+    lat = np.zeros((B * T, k + k * k), np.float32)
+    lat[:, :k] = rng.integers(0, 1 << 20, size=(B * T, k))
+    lat[:, k:] = np.round(rng.standard_normal((B * T, k * k)) * 4) / 4  # many exact ties
+    for b in range(B):
+        lat[b * T, k:] = np.tile(lat[b * T, k:2 * k], k)
+    got = host(df.dflash2_walk(dev(lat), B, T, k))
+    want, _ = oracle.walk(lat, B, T, k)
+    assert np.array_equal(got, want)
+
+
+# ---------------------------------------------------------------- whole path, edge cases
+
+
+def small_case(B, T, H, V, k, D, seed):
+    cfg = SelectorConfig("edge", B, T, H, V, k, D)
+    return cfg, make_inputs(cfg, seed)
+
+
+def run_select(x, cfg):
+    d = {n: dev_bf16(x[n]) for n in ("hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb")}
+    lat, draft = df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], dev(x["anchor"]),
+                                   cfg.k, cfg.T)
+    return host(lat), host(draft)
+
+
+@pytest.mark.parametrize("B,T,H,V,k,D", [(1, 1, 64, 16, 1, 8), (3, 7, 200, 1013, 5, 24), (2, 9, 136, 5000, 32, 64),
+                                         (9, 16, 512, 3000, 16, 128), (1, 4, 8, 32, 32, 8)])
+def test_select_edge_shapes(B, T, H, V, k, D):
+    cfg, x = small_case(B, T, H, V, k, D, seed=B + T + k)
+    lat, draft = run_select(x, cfg)
+    ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
+    tol = row_tol(ora["logits"])
+    ids = lat[:, :k].astype(np.int32)
+    check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+                           ora["topk_vals"], tol)
+    compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
+    assert compared + low >= 1
+
+
+def test_zeroed_codebooks_give_per_position_top1():
+    cfg, x = small_case(4, 6, 256, 2048, 8, 32, seed=5)
+    x["pred_cb"][:] = 0
+    lat, draft = run_select(x, cfg)
+    assert np.array_equal(draft.reshape(-1), lat[:, 0].astype(np.int32))
+    x2 = dict(x)
+    x2["succ_cb"] = np.zeros_like(x["succ_cb"])
+    x2["pred_cb"] = make_inputs(cfg, 5)["pred_cb"]
+    lat2, draft2 = run_select(x2, cfg)
+    assert np.array_equal(draft2.reshape(-1), lat2[:, 0].astype(np.int32))
+
+
+def test_k1_walk_is_top1():
+    cfg, x = small_case(3, 5, 128, 777, 1, 16, seed=9)
+    lat, draft = run_select(x, cfg)
+    ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], 1, 5)
+    assert lat.shape == (15, 2)
+    assert np.array_equal(draft.reshape(-1), lat[:, 0].astype(np.int32))
+    tol = row_tol(ora["logits"])
+    for r in range(15):
+        g = int(lat[r, 0])
+        assert ora["logits"][r, g] >= ora["topk_vals"][r, 0] - tol[r]
