@@ -263,6 +263,8 @@ def run_ours(args, cfg, rank: int, world: int):
     eb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ee = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for ev in eb + ee:  # torch creates the CUDA event on its first record(); the library needs the handle
+        ev.record()
     sampler = ClockSampler(device_id_for_smi(torch)) if rank == 0 else None
     barrier()
     torch.cuda.synchronize()

@@ -139,6 +139,21 @@ DF2_API df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidd
 DF2_API df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk_ids, float *topk_logits,
                         void *workspace, size_t workspace_bytes, void *stream);
 
+/* Top-k of given float32 logits without a workspace, for callers that cannot allocate
+ * device memory (an engine that plans all device memory itself and gives plugins no
+ * allocator; a decode loop that cannot afford cudaMalloc's implicit synchronisation).
+ * Same kernels and results as dflash2_topk; the per-slice partial lists live in an
+ * 8 MiB array inside the library's device image (held by every GPU that loads the
+ * library until exit), so B*T*KP must not exceed 4096 (KP = k rounded up to 4, 8, 16 or
+ * 32); larger requests return DF2_ERR_UNSUPPORTED.  The first call on a device looks up
+ * that array's device address (cudaGetSymbolAddress) with the device current; make that
+ * first call before any stream capture.  All calls share the array: calls that overlap on
+ * the GPU (other streams, other host threads) race and must be serialised by the caller.
+ * Every entry the kernels read is written earlier in the same call, so nothing needs
+ * clearing.  The method pages have no counterpart: this is a deployment variant. */
+DF2_API df2_status dflash2_topk_noalloc(const df2_dims *dims, const float *logits, int32_t *topk_ids,
+                                        float *topk_logits, void *stream);
+
 /* Gate alone: gate float [B*T, D] = hidden . W_sel^T, float32 accumulation on tensor cores. */
 DF2_API df2_status dflash2_gate(const df2_dims *dims, const void *hidden, const void *W_sel, float *gate, void *workspace,
                         size_t workspace_bytes, void *stream);

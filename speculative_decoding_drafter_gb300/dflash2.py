@@ -21,7 +21,7 @@ __all__ = [
     "DFlash2Error", "Dims", "library", "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select",
     "dflash2_select_from_logits", "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice",
     "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
-    "dflash2_profile_events",
+    "dflash2_profile_events", "dflash2_topk_noalloc",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -29,6 +29,7 @@ EXPORTED_SYMBOLS = (
     "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select", "dflash2_select_from_logits",
     "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
     "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
+    "dflash2_topk_noalloc",
 )
 
 
@@ -76,6 +77,7 @@ def library(path: str | None = None):
                 "dflash2_status_string": (ctypes.c_char_p, [I]),
                 "dflash2_version": (ctypes.c_int32, []),
                 "dflash2_profile_events": (I, [P, P]),
+                "dflash2_topk_noalloc": (I, [D, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -248,6 +250,20 @@ def dflash2_topk(logits, k: int, *, ids=None, vals=None, workspace=None, stream=
     return ids, vals
 
 
+def dflash2_topk_noalloc(logits, k: int, *, ids=None, vals=None, stream=None):
+    """dflash2_topk without a workspace (the library's own fixed device array holds the
+    scratch); for callers that cannot allocate.  Overlapping calls race."""
+    R, V = logits.shape
+    d = make_dims(R, 1, 8, V, k, 8)
+    ids = ids if ids is not None else torch.empty((R, k), dtype=torch.int32, device=logits.device)
+    vals = vals if vals is not None else torch.empty((R, k), dtype=torch.float32, device=logits.device)
+    st = library().dflash2_topk_noalloc(ctypes.byref(d), _ptr(logits, torch.float32, (R, V), "logits"),
+                                        _ptr(ids, torch.int32, (R, k), "topk_ids"),
+                                        _ptr(vals, torch.float32, (R, k), "topk_logits"), _stream(stream))
+    _check(st, "dflash2_topk_noalloc")
+    return ids, vals
+
+
 def dflash2_gate(hidden, W_sel, *, out=None, workspace=None, stream=None):
     """Gate float32 [R, D] = hidden . W_sel^T on tensor cores."""
     R, H = hidden.shape
@@ -301,4 +317,6 @@ def dflash2_profile_events(begin=None, end=None) -> None:
     """Record torch.cuda.Event pairs around the LM-head launch of following select calls (None, None stops)."""
     b = None if begin is None else begin.cuda_event
     e = None if end is None else end.cuda_event
+    if (begin is not None and not b) or (end is not None and not e):
+        raise ValueError("record each torch.cuda.Event once before passing it (torch creates it lazily)")
     _check(library().dflash2_profile_events(b, e), "dflash2_profile_events")
