@@ -35,7 +35,7 @@ from speculative_decoding_drafter_gb300.synth import CONFIGS, make_inputs  # noq
 
 METRIC = "selector draft rows/s and µs/block; % of HBM or bf16 tensor roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-LAUNCHES_PER_STEP = 5  # LM head + top-k, gate, merge, lattice, walk
+LAUNCHES_PER_STEP = 2  # LM head with fused top-k and gate; merge + lattice + walk
 DOMINANT_SOURCES = ["speculative_decoding_drafter_gb300/csrc/gemm_tc.cu", "speculative_decoding_drafter_gb300/csrc/ptx.cuh",
                     "speculative_decoding_drafter_gb300/csrc/topk.cuh"]
 
@@ -77,7 +77,7 @@ def roofline_bound(cfg, peaks):
 
 def dominant_source_sha() -> str:
     h = hashlib.sha256()
-    for rel in DOMINANT_SOURCES:
+    for rel in DOMINANT_SOURCES:  # the kernel's own sources
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -336,7 +336,7 @@ def run_ours(args, cfg, rank: int, world: int):
         algo = 2.0 * cfg.R * cfg.H * cfg.V
         achieved, peak, unit = algo / lm_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     roof = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-            "traffic": recorded_traffic(cfg), "kernel": "gemm_tc_kernel (LM head + fused top-k)",
+            "traffic": recorded_traffic(cfg), "kernel": "gemm_tc_kernel (LM head + fused top-k + gate)",
             "kernel_us": lm_ms * 1e3, "algorithmic_per_launch": algo, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json)"
             if peak_kind == "measured" else "fallback"}
     # the same roofline over the whole step (every launch of the call, host gaps included)

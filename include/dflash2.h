@@ -86,12 +86,16 @@ typedef struct df2_dims {
 } df2_dims;
 
 /* Bytes of device workspace the calls below need for `dims` (0 if dims are invalid).
- * The first 256 bytes hold the sticky device status word: zero them once before the
- * first call (dflash2_workspace_init).  Independent of the device. */
+ * Independent of the device.  The workspace starts with a control block (the sticky
+ * device status word and one completion counter per sequence) that must be zero before
+ * the first call: dflash2_workspace_init zeroes it (a zero-filled allocation also works).
+ * Calls leave the counters at zero, so a workspace is reused without re-initialising;
+ * after a DF2_ERR_TIMEOUT, initialise it again.  One workspace serves one stream at a time. */
 DF2_API size_t dflash2_workspace_bytes(const df2_dims *dims);
 
-/* Zeroes the device status word at the start of `workspace` (cudaMemsetAsync on stream). */
-DF2_API df2_status dflash2_workspace_init(void *workspace, size_t workspace_bytes, void *stream);
+/* Zeroes the control block at the start of `workspace` for `dims` (cudaMemsetAsync on stream). */
+DF2_API df2_status dflash2_workspace_init(const df2_dims *dims, void *workspace, size_t workspace_bytes,
+                                          void *stream);
 
 /*
  * The whole selector head (LM head + top-k, gate, lattice, walk) for B*T rows.
@@ -107,8 +111,9 @@ DF2_API df2_status dflash2_workspace_init(void *workspace, size_t workspace_byte
  *   topk_ids int32 [B*T, k], topk_logits float [B*T, k], gate float [B*T, D]:
  *            optional copies of the candidates (sorted by logit desc, id asc), their
  *            logits (the unary scores) and the gate; NULL to skip.
- * The full float32 logits never reach global memory: each CTA of the tensor-core
- * LM head keeps a per-row top-k of its vocabulary slice in registers.
+ * Two launches: the tensor-core LM head (which also computes the gate) and one kernel
+ * for the merge, lattice and walk.  The full float32 logits never reach global memory:
+ * each CTA of the LM head keeps a per-row top-k of its vocabulary slice in registers.
  */
 DF2_API df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *W_vocab, const void *W_sel,
                           const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,

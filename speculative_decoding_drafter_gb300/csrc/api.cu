@@ -52,16 +52,19 @@ df2_status check_dims(const df2_dims *d)
 
 struct Workspace {
     uint32_t *status;
+    unsigned *counters;
     float *pval;
     int32_t *pid;
-    int32_t *topk_ids;
-    float *topk_vals;
+    int32_t *best;
     float *gate;
     size_t bytes;
 };
 
-// Layout (each part 256-byte aligned): status word | partial values | partial ids |
-// top-k ids | top-k values | gate.
+// Control block (zeroed by dflash2_workspace_init): status word, per-sequence counters.
+size_t control_bytes(const df2_dims &d) { return kAlign + round_up(sizeof(unsigned) * static_cast<size_t>(d.B)); }
+
+// Layout (each part 256-byte aligned): status word | sequence counters | partial values |
+// partial ids | walk choices | gate.
 Workspace carve(const df2_dims &d, void *base)
 {
     const size_t R = static_cast<size_t>(d.B) * d.T;
@@ -71,14 +74,14 @@ Workspace carve(const df2_dims &d, void *base)
     size_t off = 0;
     w.status = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
     off += kAlign;
+    w.counters = reinterpret_cast<unsigned *>(p ? p + off : nullptr);
+    off += round_up(sizeof(unsigned) * static_cast<size_t>(d.B));
     w.pval = reinterpret_cast<float *>(p ? p + off : nullptr);
     off += round_up(R * kMaxSplits * kp * sizeof(float));
     w.pid = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
     off += round_up(R * kMaxSplits * kp * sizeof(int32_t));
-    w.topk_ids = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
+    w.best = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
     off += round_up(R * d.k * sizeof(int32_t));
-    w.topk_vals = reinterpret_cast<float *>(p ? p + off : nullptr);
-    off += round_up(R * d.k * sizeof(float));
     w.gate = reinterpret_cast<float *>(p ? p + off : nullptr);
     off += round_up(R * d.D * sizeof(float));
     w.bytes = off;
@@ -111,14 +114,14 @@ cudaError_t profile_mark(cudaEvent_t ev, cudaStream_t st) { return ev ? cudaEven
 
 #define DF2_CUDA(expr) DF2_TRY(from_cuda(expr))
 
-// Shared tail of both select paths: lattice then walk.
-df2_status lattice_and_walk(const df2_dims &d, const int32_t *ids, const float *vals, const float *gate,
-                            const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,
-                            int32_t *draft_ids, cudaStream_t st)
+// Shared tail of both select paths: merge, lattice and walk in one launch.
+df2_status finish(const df2_dims &d, const Workspace &w, int n_split, const float *gate, const void *pred_cb,
+                  const void *succ_cb, const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
+                  float *topk_vals, cudaStream_t st)
 {
-    DF2_CUDA(launch_lattice(d.B, d.T, d.k, d.V, d.D, ids, vals, gate, static_cast<const uint16_t *>(pred_cb),
-                            static_cast<const uint16_t *>(succ_cb), anchor, lattice, st));
-    DF2_CUDA(launch_walk(d.B, d.T, d.k, lattice, draft_ids, st));
+    DF2_CUDA(launch_finish(d.B, d.T, d.k, d.V, d.D, kp_for(d.k), n_split, w.pval, w.pid, gate,
+                           static_cast<const uint16_t *>(pred_cb), static_cast<const uint16_t *>(succ_cb), anchor,
+                           lattice, draft_ids, topk_ids, topk_vals, w.best, w.counters, st));
     return DF2_OK;
 }
 
@@ -151,11 +154,12 @@ size_t dflash2_workspace_bytes(const df2_dims *dims)
     return carve(*dims, nullptr).bytes;
 }
 
-df2_status dflash2_workspace_init(void *workspace, size_t workspace_bytes, void *stream)
+df2_status dflash2_workspace_init(const df2_dims *dims, void *workspace, size_t workspace_bytes, void *stream)
 {
-    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < kAlign)
-        return DF2_ERR_WORKSPACE;
-    return from_cuda(cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)));
+    DF2_TRY(check_dims(dims));
+    DF2_TRY(check_workspace(*dims, workspace, workspace_bytes));
+    return from_cuda(
+        cudaMemsetAsync(workspace, 0, control_bytes(*dims), static_cast<cudaStream_t>(stream)));
 }
 
 df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *W_vocab, const void *W_sel,
@@ -174,16 +178,13 @@ df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int R = d.B * d.T;
     const int kp = kp_for(d.k);
-    int32_t *ids = topk_ids ? topk_ids : w.topk_ids;
-    float *vals = topk_logits ? topk_logits : w.topk_vals;
     float *g = gate ? gate : w.gate;
     int n_split = 0;
     DF2_CUDA(profile_mark(t_profile_begin, st));
-    DF2_CUDA(launch_gemm_topk(hidden, W_vocab, R, d.H, d.V, kp, w.pval, w.pid, &n_split, w.status, st));
+    DF2_CUDA(launch_lm_head(hidden, R, d.H, W_vocab, d.V, kp, w.pval, w.pid, &n_split, W_sel, d.D, g, d.D, w.status,
+                            st));
     DF2_CUDA(profile_mark(t_profile_end, st));
-    DF2_CUDA(launch_gemm_store(hidden, W_sel, R, d.H, d.D, g, d.D, w.status, st));
-    DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, ids, vals, st));
-    return lattice_and_walk(d, ids, vals, g, pred_cb, succ_cb, anchor, lattice, draft_ids, st);
+    return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st);
 }
 
 df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits, const void *hidden,
@@ -203,16 +204,13 @@ df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits,
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int R = d.B * d.T;
     const int kp = kp_for(d.k);
-    int32_t *ids = topk_ids ? topk_ids : w.topk_ids;
-    float *vals = topk_logits ? topk_logits : w.topk_vals;
     float *g = gate ? gate : w.gate;
     int n_split = 0;
     DF2_CUDA(profile_mark(t_profile_begin, st));
     DF2_CUDA(launch_logits_topk_partial(logits, R, d.V, kp, w.pval, w.pid, &n_split, st));
     DF2_CUDA(profile_mark(t_profile_end, st));
     DF2_CUDA(launch_gemm_store(hidden, W_sel, R, d.H, d.D, g, d.D, w.status, st));
-    DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, ids, vals, st));
-    return lattice_and_walk(d, ids, vals, g, pred_cb, succ_cb, anchor, lattice, draft_ids, st);
+    return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st);
 }
 
 df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidden, const void *W_vocab, float *logits,

@@ -1,0 +1,238 @@
+// finish.cu -- everything after the LM head, in one launch: merge of the per-slice
+// top-k lists, the lattice row of each draft position, and the greedy walk.
+//
+// One CTA per draft position r = b*T + t (256 threads):
+//   1. warp 0 merges the partial lists of row r into its top-k (candidates and unary
+//      scores), warp 1 those of row r-1 (the predecessors; the anchor at t = 0): lane l
+//      takes lists l, l+32, ... (each already sorted), then a warp butterfly finishes
+//      with fixed-cost bitonic merges.  Warps 2-7 meanwhile fetch the gate row;
+//   2. the lattice row (lattice.cuh), plus the walk's choice for every predecessor row;
+//   3. the CTA counts itself done for sequence b; the last CTA of the sequence loads the
+//      T choice rows and candidate ids into shared memory and follows j_t = best[t][j_(t-1)].
+//      The counter returns to zero.
+// Launched with programmatic stream serialisation: its prologue overlaps the tail of the
+// kernel that produced the lists, and griddep_wait() orders the reads after it.
+#include <cstdint>
+
+#include "internal.h"
+#include "lattice.cuh"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace df2 {
+namespace {
+
+struct FinishArgs {
+    int T, k, V, D, n_split;
+    const float *pval;
+    const int32_t *pid;
+    const float *gate;
+    const uint16_t *pred_cb;
+    const uint16_t *succ_cb;
+    const int32_t *anchor;
+    float *lattice;
+    int32_t *draft;
+    int32_t *topk_ids;   // optional copies (may be null)
+    float *topk_vals;
+    int32_t *best;       // [B*T, k] walk choices
+    unsigned *counters;  // [B], zero between calls
+    int walk_in_smem;    // the sequence's choice table fits the dynamic shared memory
+};
+
+template <int KP>
+__global__ void __launch_bounds__(kLatticeThreads) finish_kernel(const FinishArgs a)
+{
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ int s_cand[32];
+    __shared__ int s_prev[32];
+    __shared__ float s_unary[32];
+    __shared__ int s_last;
+
+    griddep_wait();
+
+    const int r = blockIdx.x;
+    const int b = r / a.T;
+    const int t = r - b * a.T;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int k = a.k;
+
+    // ---- 1. merge (warp 0: row r, warp 1: row r-1) while warps 2-7 fetch the gate row
+    if (warp < 2 && (warp == 0 || t > 0)) {
+        const long long row_base = static_cast<long long>(warp == 0 ? r : r - 1) * a.n_split * KP;
+        float av[KP];
+        int ai[KP];
+#pragma unroll
+        for (int s = 0; s < KP; ++s) {
+            av[s] = -INFINITY;
+            ai[s] = INT_MAX;
+        }
+        // several lists per lane per round, all loads issued before the merges
+        constexpr int kLists = KP <= 8 ? 5 : KP <= 16 ? 2 : 1;
+        for (int list0 = lane; list0 < a.n_split; list0 += 32 * kLists) {
+            float bv[kLists][KP];
+            int bi[kLists][KP];
+#pragma unroll
+            for (int u = 0; u < kLists; ++u) {
+                const int list = list0 + 32 * u;
+                const bool have = list < a.n_split;
+                const long long off = row_base + static_cast<long long>(have ? list : 0) * KP;
+                const float4 *pv = reinterpret_cast<const float4 *>(a.pval + off);
+                const int4 *pi = reinterpret_cast<const int4 *>(a.pid + off);
+#pragma unroll
+                for (int q = 0; q < KP / 4; ++q) {
+                    const float4 v4 = __ldcg(pv + q);
+                    const int4 i4 = __ldcg(pi + q);
+                    bv[u][4 * q] = have ? v4.x : -INFINITY;
+                    bv[u][4 * q + 1] = have ? v4.y : -INFINITY;
+                    bv[u][4 * q + 2] = have ? v4.z : -INFINITY;
+                    bv[u][4 * q + 3] = have ? v4.w : -INFINITY;
+                    bi[u][4 * q] = have ? i4.x : INT_MAX;
+                    bi[u][4 * q + 1] = have ? i4.y : INT_MAX;
+                    bi[u][4 * q + 2] = have ? i4.z : INT_MAX;
+                    bi[u][4 * q + 3] = have ? i4.w : INT_MAX;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kLists; ++u)
+                merge_top<KP>(av, ai, bv[u], bi[u]);
+        }
+        warp_merge_top<KP>(av, ai, 31);
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < KP; ++s) {
+                if (s < k) {
+                    if (warp == 0) {
+                        s_cand[s] = clamp_id(ai[s], a.V);
+                        s_unary[s] = av[s];
+                    } else {
+                        s_prev[s] = clamp_id(ai[s], a.V);
+                    }
+                }
+            }
+        }
+    } else if (warp >= 2) {
+        load_gate_row(reinterpret_cast<float *>(smem), a.gate + static_cast<long long>(r) * a.D, a.D, 64,
+                      blockDim.x - 64);
+    }
+    if (t == 0 && threadIdx.x == 0)
+        s_prev[0] = clamp_id(a.anchor[b], a.V);
+    __syncthreads();
+    if (threadIdx.x < k) {
+        const long long o = static_cast<long long>(r) * k + threadIdx.x;
+        if (a.topk_ids)
+            a.topk_ids[o] = s_cand[threadIdx.x];
+        if (a.topk_vals)
+            a.topk_vals[o] = s_unary[threadIdx.x];
+    }
+
+    // ---- 2. lattice row and the walk's choice from each predecessor row
+    const long long width = k + static_cast<long long>(k) * k;
+    lattice_row<KP>(k, a.D, t == 0 ? 1 : k, s_prev, s_cand, s_unary, a.pred_cb, a.succ_cb, smem,
+                    a.lattice + r * width, a.best + static_cast<long long>(r) * k);
+
+    // ---- 3. the last CTA of the sequence walks it
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(a.counters + b, 1u) == static_cast<unsigned>(a.T - 1);
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    const long long r0 = static_cast<long long>(b) * a.T;
+    const int32_t *best = a.best + r0 * k;
+    const float *rows = a.lattice + r0 * width;
+    int32_t *draft = a.draft + r0;
+    if (a.walk_in_smem) {
+        int *sb = reinterpret_cast<int *>(smem);     // [T][k] choices
+        int *sid = sb + a.T * k;                     // [T][k] candidate ids
+        for (int i = threadIdx.x; i < a.T * k; i += blockDim.x) {
+            const int tt = i / k, j = i - tt * k;
+            sb[i] = __ldcg(best + i);
+            sid[i] = static_cast<int>(__ldcg(rows + tt * width + j));
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int j = 0;
+            for (int tt = 0; tt < a.T; ++tt) {
+                j = sb[tt * k + j];
+                draft[tt] = sid[tt * k + j];
+            }
+        }
+    } else if (threadIdx.x == 0) {
+        int j = 0;
+        for (int tt = 0; tt < a.T; ++tt) {
+            j = __ldcg(best + static_cast<long long>(tt) * k + j);
+            draft[tt] = static_cast<int32_t>(__ldcg(rows + tt * width + j));
+        }
+    }
+    if (threadIdx.x == 0)
+        a.counters[b] = 0u;
+}
+
+constexpr size_t kWalkSmemCap = 64 * 1024;
+
+template <int KP>
+cudaError_t launch_kp(FinishArgs a, int B, cudaStream_t stream)
+{
+    const size_t walk_bytes = 2 * sizeof(int) * static_cast<size_t>(a.T) * a.k;
+    a.walk_in_smem = walk_bytes <= kWalkSmemCap;
+    size_t smem = lattice_smem_bytes(a.k, a.D);
+    if (a.walk_in_smem && walk_bytes > smem)
+        smem = walk_bytes;
+    cudaError_t e = cudaFuncSetAttribute(finish_kernel<KP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(B * a.T));
+    cfg.blockDim = dim3(kLatticeThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, finish_kernel<KP>, a);
+    if (e != cudaSuccess)
+        return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_finish(int B, int T, int k, int V, int D, int KP, int n_split, const float *pval,
+                          const int32_t *pid, const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
+                          const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
+                          float *topk_vals, int32_t *best, unsigned *counters, cudaStream_t stream)
+{
+    FinishArgs a{};
+    a.T = T;
+    a.k = k;
+    a.V = V;
+    a.D = D;
+    a.n_split = n_split;
+    a.pval = pval;
+    a.pid = pid;
+    a.gate = gate;
+    a.pred_cb = pred_cb;
+    a.succ_cb = succ_cb;
+    a.anchor = anchor;
+    a.lattice = lattice;
+    a.draft = draft_ids;
+    a.topk_ids = topk_ids;
+    a.topk_vals = topk_vals;
+    a.best = best;
+    a.counters = counters;
+    switch (KP) {
+    case 4: return launch_kp<4>(a, B, stream);
+    case 8: return launch_kp<8>(a, B, stream);
+    case 16: return launch_kp<16>(a, B, stream);
+    case 32: return launch_kp<32>(a, B, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace df2

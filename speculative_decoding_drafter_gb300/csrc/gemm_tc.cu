@@ -1,22 +1,26 @@
-// gemm_tc.cu -- the selector head's LM head (and gate) on tcgen05 tensor cores.
+// gemm_tc.cu -- the selector head's LM head and gate on tcgen05 tensor cores.
 //
-// C[R, N] = A[R, K] . B[N, K]^T with A = hidden states (bf16, K = H) and B = the
-// LM-head rows W_vocab (N = V) or the selector projection W_sel (N = D).
-// "DFlash 2: Keep Drafting Parallel", section "A Lightweight Path Selector": the
-// unary score of a candidate is the drafter's own logit; the gate H(h_t) is a
-// projection of the same hidden state.
+// C[R, n] = A[R, K] . B[n, K]^T with A = hidden states (bf16, K = H).  One launch covers
+// two column segments of C:
+//   top-k segment  B = W_vocab (n = V): "DFlash 2: Keep Drafting Parallel", section "A
+//                  Lightweight Path Selector" -- the unary score of a candidate is the
+//                  drafter's own logit; only a per-row top-k of these columns is kept;
+//   store segment  B = W_sel (n = D): the context gate H(h_t), a projection of the same
+//                  hidden state, stored as float32.
+// Either segment may be empty (the stage entry points use the store segment alone).
 //
 // Design (one CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: 128-row tiles of A and up-to-256-row tiles of B,
-//               64 K-elements (128 bytes, 128-byte swizzle) per stage, 4 stages.
+//   warp 0      TMA producer: an A box of the live rows (<= 128) and up to 256 rows of B,
+//               64 K-elements (128 bytes, 128-byte swizzle) per stage, 4-6 stages.
 //   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N<=256,
 //               K=16 per instruction) into one of two 256-column accumulators.
-//   warps 2-5   epilogue: tcgen05.ld the accumulator (thread = one row of C),
-//               then either keep a per-row top-KP list in registers (the LM head:
-//               full logits never reach global memory) or store float32 (gate).
-// Work split: CTA (m, s) owns row tile m and a contiguous slice of C's columns
-// (multiples of 16), walked in chunks of 256.  CTAs sharing a slice are launched
-// next to each other, so W_vocab is read from HBM about once and re-read from L2.
+//   warps 2-5   epilogue: tcgen05.ld the accumulator (thread = one row of C), then keep
+//               a per-row top-KP list in registers (full logits never reach global
+//               memory) or store float32.
+// Work split: CTA (m, s) owns row tile m and a contiguous slice of the columns of both
+// segments (multiples of 16), walked in chunks of <= 256 that never straddle the segment
+// boundary.  CTAs sharing a slice are launched next to each other, so W_vocab is read
+// from HBM about once and re-read from L2 by the other row tiles.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -34,24 +38,81 @@ constexpr int BM = 128;                        // rows of C per tile = TMEM lane
 constexpr int BN = 256;                        // columns of C per chunk (MMA N, max)
 constexpr int BK = 64;                         // K elements per stage: one 128-byte swizzle row
 constexpr int UNIT = 16;                       // column granularity of slices and of MMA N
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;           // 16 KB
+constexpr int MAX_STAGES = 8;
+constexpr int A_TILE_BYTES = BM * BK * 2;      // what one MMA reads of A: 16 KB
 constexpr int B_BYTES = BN * BK * 2;           // 32 KB
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int STASH_STRIDE = 33;               // floats per epilogue thread (32 + 1 pad)
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * (A_BYTES + B_BYTES) + BAR_BYTES + BM * STASH_STRIDE * 4;
+constexpr int STASH_BYTES = BM * STASH_STRIDE * 4;
+constexpr int SMEM_LIMIT = 227 * 1024;
+constexpr int STAGE_BUDGET = SMEM_LIMIT - 1024 - BAR_BYTES - STASH_BYTES;
 
 struct GemmArgs {
-    int R, K, N;
+    int R, K;
+    int n_topk;       // columns of the top-k segment
+    int n_topk_pad;   // rounded up to UNIT: start of the store segment in the column space
+    int n_store;      // columns of the store segment
     int row_tiles, n_split;
-    float *pval;     // top-k mode: [R, n_split, KP]
+    int stages;       // pipeline depth
+    int a_bytes;      // bytes of one A box (live rows x 128), a multiple of 1024
+    float *pval;      // top-k lists [R, n_split, KP]
     int32_t *pid;
-    float *out;      // store mode: out[r * ldo + n]
+    float *out;       // store segment: out[r * ldo + n]
     long long ldo;
     uint32_t *status;
 };
+
+// One chunk of a CTA's column slice.
+struct Chunk {
+    int c0;       // first column in the joint column space
+    int n;        // columns (a multiple of UNIT, <= BN)
+    bool store;   // store segment?
+    int b_row;    // first row of the segment's B matrix
+    int valid;    // columns of the chunk that exist in the segment (<= n)
+};
+
+struct Slice {
+    int a0, a1;   // top-k segment part [a0, a1)
+    int b0, b1;   // store segment part [b0, b1)
+    int n0, n1;   // chunks in each part
+};
+
+__device__ __forceinline__ Slice slice_of(const GemmArgs &g, int split)
+{
+    const int total_units = (g.n_topk_pad + g.n_store + UNIT - 1) / UNIT;
+    const int u0 = static_cast<int>(static_cast<long long>(split) * total_units / g.n_split);
+    const int u1 = static_cast<int>(static_cast<long long>(split + 1) * total_units / g.n_split);
+    Slice s;
+    const int c_begin = u0 * UNIT, c_end = u1 * UNIT;
+    s.a0 = c_begin;
+    s.a1 = min(c_end, g.n_topk_pad);
+    s.b0 = max(c_begin, g.n_topk_pad);
+    s.b1 = c_end;
+    s.n0 = s.a1 > s.a0 ? (s.a1 - s.a0 + BN - 1) / BN : 0;
+    s.n1 = s.b1 > s.b0 ? (s.b1 - s.b0 + BN - 1) / BN : 0;
+    return s;
+}
+
+__device__ __forceinline__ Chunk chunk_of(const GemmArgs &g, const Slice &s, int c)
+{
+    Chunk ch;
+    if (c < s.n0) {
+        ch.c0 = s.a0 + c * BN;
+        ch.n = min(BN, s.a1 - ch.c0);
+        ch.store = false;
+        ch.b_row = ch.c0;
+        ch.valid = max(0, min(ch.n, g.n_topk - ch.c0));
+    } else {
+        ch.c0 = s.b0 + (c - s.n0) * BN;
+        ch.n = min(BN, s.b1 - ch.c0);
+        ch.store = true;
+        ch.b_row = ch.c0 - g.n_topk_pad;
+        ch.valid = max(0, min(ch.n, g.n_store - ch.b_row));
+    }
+    return ch;
+}
 
 // Waits without looking at the abort flag; used only to drain in-flight work after an abort.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
@@ -62,42 +123,40 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
             return;
 }
 
-template <int KP, bool kStore>
+template <int KP>
 __global__ void __launch_bounds__(THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b_wide,
-                   const __grid_constant__ CUtensorMap map_b_narrow, const GemmArgs args)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_t_wide,
+                   const __grid_constant__ CUtensorMap map_t_narrow, const __grid_constant__ CUtensorMap map_s_wide,
+                   const __grid_constant__ CUtensorMap map_s_narrow, const GemmArgs args)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = smem;
-    uint8_t *sB = smem + STAGES * A_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
-    // bars: full[STAGES] | empty[STAGES] | tfull[2] | tempty[2] | drain
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * STAGES + 5);
+    const int stages = args.stages;
+    const int stage_bytes = args.a_bytes + B_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
+    // bars: full[MAX_STAGES] | empty[MAX_STAGES] | tfull[2] | tempty[2] | drain
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * MAX_STAGES + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *stash = reinterpret_cast<float *>(sB + STAGES * B_BYTES + BAR_BYTES);
+    float *stash = reinterpret_cast<float *>(smem + stages * stage_bytes + BAR_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int m_tile = blockIdx.x % args.row_tiles;
     const int split = blockIdx.x / args.row_tiles;
-    const int units = (args.N + UNIT - 1) / UNIT;
-    const int u0 = static_cast<int>(static_cast<long long>(split) * units / args.n_split);
-    const int u1 = static_cast<int>(static_cast<long long>(split + 1) * units / args.n_split);
-    const int col_begin = u0 * UNIT;
-    const int col_end = min(u1 * UNIT, args.N);
-    const int n_chunks = col_end > col_begin ? (col_end - col_begin + BN - 1) / BN : 0;
+    const Slice slice = slice_of(args, split);
+    const int n_chunks = slice.n0 + slice.n1;
     const int kblocks = (args.K + BK - 1) / BK;
 
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
-    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (MAX_STAGES + s); };
+    auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * MAX_STAGES + b); };
+    auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * MAX_STAGES + 2 + b); };
+    const uint32_t drain_bar = bar0 + 8u * (2 * MAX_STAGES + 4);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        griddep_launch_dependents();
+        for (int s = 0; s < stages; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -109,8 +168,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&map_a);
-        prefetch_tmap(&map_b_wide);
-        prefetch_tmap(&map_b_narrow);
+        if (slice.n0) {
+            prefetch_tmap(&map_t_wide);
+            prefetch_tmap(&map_t_narrow);
+        }
+        if (slice.n1) {
+            prefetch_tmap(&map_s_wide);
+            prefetch_tmap(&map_s_narrow);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -129,27 +194,28 @@ __global__ void __launch_bounds__(THREADS, 1)
             long long issued = 0;
             bool ok = true;
             for (int c = 0; c < n_chunks && ok; ++c) {
-                const int c0 = col_begin + c * BN;
-                const int nc = min(BN, col_end - c0);
-                const int nmma = (nc + UNIT - 1) / UNIT * UNIT;
-                const uint32_t tx = static_cast<uint32_t>(A_BYTES + nmma * BK * 2);
+                const Chunk ch = chunk_of(args, slice, c);
+                const CUtensorMap *wide = ch.store ? &map_s_wide : &map_t_wide;
+                const CUtensorMap *narrow = ch.store ? &map_s_narrow : &map_t_narrow;
+                const uint32_t tx = static_cast<uint32_t>(args.a_bytes + ch.n * BK * 2);
                 for (int kb = 0; kb < kblocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    uint8_t *st = smem + stage * stage_bytes;
                     mbar_arrive_expect_tx(full_bar(stage), tx);
-                    tma_load_2d(smem_u32(sA + stage * A_BYTES), &map_a, full_bar(stage), kb * BK, m_tile * BM);
-                    const uint32_t b_dst = smem_u32(sB + stage * B_BYTES);
-                    if (nmma == BN) {
-                        tma_load_2d(b_dst, &map_b_wide, full_bar(stage), kb * BK, c0);
+                    tma_load_2d(smem_u32(st), &map_a, full_bar(stage), kb * BK, m_tile * BM);
+                    const uint32_t b_dst = smem_u32(st + args.a_bytes);
+                    if (ch.n == BN) {
+                        tma_load_2d(b_dst, wide, full_bar(stage), kb * BK, ch.b_row);
                     } else {
-                        for (int q = 0; q < nmma / UNIT; ++q)
-                            tma_load_2d(b_dst + q * UNIT * BK * 2, &map_b_narrow, full_bar(stage), kb * BK,
-                                        c0 + q * UNIT);
+                        for (int q = 0; q < ch.n / UNIT; ++q)
+                            tma_load_2d(b_dst + q * UNIT * BK * 2, narrow, full_bar(stage), kb * BK,
+                                        ch.b_row + q * UNIT);
                     }
                     ++issued;
-                    if (++stage == STAGES) {
+                    if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -157,9 +223,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {
                 // let the copies already issued land before the CTA leaves
-                const long long first = issued > STAGES ? issued - STAGES : 0;
+                const long long first = issued > stages ? issued - stages : 0;
                 for (long long n = first; n < issued; ++n)
-                    drain_wait(full_bar(static_cast<int>(n % STAGES)), static_cast<uint32_t>((n / STAGES) & 1));
+                    drain_wait(full_bar(static_cast<int>(n % stages)), static_cast<uint32_t>((n / stages) & 1));
             }
         }
     } else if (warp == 1) {
@@ -171,10 +237,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int c = 0; c < n_chunks && ok; ++c) {
                 const int buf = c & 1;
                 const uint32_t use = static_cast<uint32_t>(c >> 1);
-                const int c0 = col_begin + c * BN;
-                const int nc = min(BN, col_end - c0);
-                const int nmma = (nc + UNIT - 1) / UNIT * UNIT;
-                const uint32_t idesc = idesc_bf16_f32(BM, nmma);
+                const Chunk ch = chunk_of(args, slice, c);
+                const uint32_t idesc = idesc_bf16_f32(BM, ch.n);
                 if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -187,14 +251,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sA + stage * A_BYTES);
-                    const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
+                    const uint32_t a0 = smem_u32(smem + stage * stage_bytes);
+                    const uint32_t b0 = a0 + static_cast<uint32_t>(args.a_bytes);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         umma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
                                   (kb | kk) != 0 ? 1u : 0u);
                     umma_commit(empty_bar(stage));
-                    if (++stage == STAGES) {
+                    if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -219,23 +283,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < n_chunks; ++c) {
             const int buf = c & 1;
             const uint32_t use = static_cast<uint32_t>(c >> 1);
-            const int c0 = col_begin + c * BN;
-            const int nc = min(BN, col_end - c0);
+            const Chunk ch = chunk_of(args, slice, c);
             const bool ready = mbar_wait(tfull_bar(buf), use & 1u, abort_flag);
             if (!__all_sync(kFullMask, ready))
                 break;
             tc_fence_after();
-            for (int cb = 0; cb < (nc + 31) / 32; ++cb) {
+            for (int cb = 0; cb < ch.n / 32 + ((ch.n & 31) ? 1 : 0); ++cb) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + cb * 32),
                                    r);
                 tmem_wait_ld(r);
-                const int base_col = c0 + cb * 32;
-                const int valid = min(32, col_end - base_col);
-                if constexpr (kStore) {
-                    if (row_ok) {
-                        float *dst = args.out + static_cast<long long>(row) * args.ldo + base_col;
+                const int valid = min(32, ch.valid - cb * 32);
+                if (ch.store) {
+                    if (row_ok && valid > 0) {
+                        float *dst = args.out + static_cast<long long>(row) * args.ldo + (ch.b_row + cb * 32);
                         if (valid == 32 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
 #pragma unroll
                             for (int j = 0; j < 32; j += 4)
@@ -249,24 +311,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     dst[j] = __uint_as_float(r[j]);
                         }
                     }
-                } else {
-                    if (row_ok) {
-                        const float thr = top.threshold();
-                        uint32_t mask = 0;
+                } else if (row_ok && valid > 0) {
+                    const float thr = top.threshold();
+                    uint32_t mask = 0;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        mask |= static_cast<uint32_t>(__uint_as_float(r[j]) > thr) << j;
+                    if (valid < 32)
+                        mask &= (1u << valid) - 1u;
+                    if (mask) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            mask |= static_cast<uint32_t>(__uint_as_float(r[j]) > thr) << j;
-                        if (valid < 32)
-                            mask &= (1u << valid) - 1u;
-                        if (mask) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                my_stash[j] = __uint_as_float(r[j]);
-                            while (mask) {
-                                const int j = __ffs(mask) - 1;
-                                mask &= mask - 1u;
-                                top.push_increasing_id(my_stash[j], base_col + j);
-                            }
+                            my_stash[j] = __uint_as_float(r[j]);
+                        const int base_col = ch.c0 + cb * 32;
+                        while (mask) {
+                            const int j = __ffs(mask) - 1;
+                            mask &= mask - 1u;
+                            top.push_increasing_id(my_stash[j], base_col + j);
                         }
                     }
                 }
@@ -274,14 +335,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before();
             mbar_arrive(tempty_bar(buf));
         }
-        if constexpr (!kStore) {
-            if (row_ok) {
-                const long long base = (static_cast<long long>(row) * args.n_split + split) * KP;
+        if (row_ok && args.n_topk > 0) {
+            const long long base = (static_cast<long long>(row) * args.n_split + split) * KP;
 #pragma unroll
-                for (int s = 0; s < KP; ++s) {
-                    args.pval[base + s] = top.v[s];
-                    args.pid[base + s] = top.i[s];
-                }
+            for (int s = 0; s < KP; ++s) {
+                args.pval[base + s] = top.v[s];
+                args.pid[base + s] = top.i[s];
             }
         }
     }
@@ -327,49 +386,68 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int KP, bool kStore>
-cudaError_t launch(const void *A, const void *B, int R, int K, int N, GemmArgs args, int *n_split_out,
-                   cudaStream_t stream)
+template <int KP>
+cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, const void *Bs, int n_store,
+                   GemmArgs args, int *n_split_out, cudaStream_t stream)
 {
-    CUtensorMap ma, mbw, mbn;
+    // A box: the live rows of a tile, rounded to 8 (one swizzle atom); the MMA still reads
+    // 128 rows, the rows past the box hold stale shared memory and only feed unused rows of C.
+    const int a_rows = std::min(BM, (std::max(R, 1) + 7) / 8 * 8);
+    args.a_bytes = a_rows * BK * 2;
+    const int stage_bytes = args.a_bytes + B_BYTES;
+    args.stages = std::min(MAX_STAGES, STAGE_BUDGET / stage_bytes);
+    if (args.stages < 2 || stage_bytes < A_TILE_BYTES)
+        return cudaErrorInvalidConfiguration;
+    const int smem_bytes = 1024 + args.stages * stage_bytes + BAR_BYTES + STASH_BYTES;
+
+    CUtensorMap ma, mtw, mtn, msw, msn;
     cudaError_t e;
-    if ((e = make_map(&ma, A, K, R, BM)) != cudaSuccess)
+    if ((e = make_map(&ma, A, K, R, a_rows)) != cudaSuccess)
         return e;
-    if ((e = make_map(&mbw, B, K, N, BN)) != cudaSuccess)
+    // an empty segment gets the other segment's maps (never read)
+    const void *tb = n_topk > 0 ? Bt : Bs;
+    const int tn = n_topk > 0 ? n_topk : n_store;
+    const void *sb = n_store > 0 ? Bs : Bt;
+    const int sn = n_store > 0 ? n_store : n_topk;
+    if ((e = make_map(&mtw, tb, K, tn, BN)) != cudaSuccess || (e = make_map(&mtn, tb, K, tn, UNIT)) != cudaSuccess ||
+        (e = make_map(&msw, sb, K, sn, BN)) != cudaSuccess || (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
         return e;
-    if ((e = make_map(&mbn, B, K, N, UNIT)) != cudaSuccess)
-        return e;
-    auto kern = gemm_tc_kernel<KP, kStore>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES)) != cudaSuccess)
+    auto kern = gemm_tc_kernel<KP>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
         return e;
     const int sms = device_sm_count();
-    const int units = (N + UNIT - 1) / UNIT;
     args.R = R;
     args.K = K;
-    args.N = N;
+    args.n_topk = n_topk;
+    args.n_topk_pad = (n_topk + UNIT - 1) / UNIT * UNIT;
+    args.n_store = n_store;
+    const int units = (args.n_topk_pad + n_store + UNIT - 1) / UNIT;
     args.row_tiles = (R + BM - 1) / BM;
     args.n_split = std::max(1, std::min({kMaxSplits, units, std::max(1, sms / args.row_tiles)}));
     if (n_split_out)
         *n_split_out = args.n_split;
     const dim3 grid(static_cast<unsigned>(args.row_tiles * args.n_split));
-    gemm_tc_kernel<KP, kStore><<<grid, THREADS, SMEM_BYTES, stream>>>(ma, mbw, mbn, args);
+    gemm_tc_kernel<KP><<<grid, THREADS, smem_bytes, stream>>>(ma, mtw, mtn, msw, msn, args);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_topk(const void *A, const void *B, int R, int K, int N, int KP, float *pval, int32_t *pid,
-                             int *n_split_out, uint32_t *status, cudaStream_t stream)
+cudaError_t launch_lm_head(const void *hidden, int R, int K, const void *W_vocab, int V, int KP, float *pval,
+                           int32_t *pid, int *n_split_out, const void *W_store, int n_store, float *out,
+                           long long ldo, uint32_t *status, cudaStream_t stream)
 {
     GemmArgs a{};
     a.pval = pval;
     a.pid = pid;
+    a.out = out;
+    a.ldo = ldo;
     a.status = status;
     switch (KP) {
-    case 4: return launch<4, false>(A, B, R, K, N, a, n_split_out, stream);
-    case 8: return launch<8, false>(A, B, R, K, N, a, n_split_out, stream);
-    case 16: return launch<16, false>(A, B, R, K, N, a, n_split_out, stream);
-    case 32: return launch<32, false>(A, B, R, K, N, a, n_split_out, stream);
+    case 4: return launch<4>(hidden, R, K, W_vocab, V, W_store, n_store, a, n_split_out, stream);
+    case 8: return launch<8>(hidden, R, K, W_vocab, V, W_store, n_store, a, n_split_out, stream);
+    case 16: return launch<16>(hidden, R, K, W_vocab, V, W_store, n_store, a, n_split_out, stream);
+    case 32: return launch<32>(hidden, R, K, W_vocab, V, W_store, n_store, a, n_split_out, stream);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -381,7 +459,7 @@ cudaError_t launch_gemm_store(const void *A, const void *B, int R, int K, int N,
     a.out = out;
     a.ldo = ldo;
     a.status = status;
-    return launch<4, true>(A, B, R, K, N, a, nullptr, stream);
+    return launch<4>(A, R, K, nullptr, 0, B, N, a, nullptr, stream);
 }
 
 }  // namespace df2

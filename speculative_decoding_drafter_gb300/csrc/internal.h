@@ -17,13 +17,16 @@ inline int kp_for(int k) { return k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32; }
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
-// C[R, N] = A[R, K] . B[N, K]^T on tensor cores (bf16 in, float32 accumulate), reduced
-// on the fly to per-row top-KP lists over each CTA's column slice:
-// pval/pid [R, n_split, KP] (value desc, id asc).  *n_split_out receives the split count.
-cudaError_t launch_gemm_topk(const void *A, const void *B, int R, int K, int N, int KP, float *pval, int32_t *pid,
-                             int *n_split_out, uint32_t *status, cudaStream_t stream);
+// LM head (and gate) in one tensor-core launch: C = hidden[R, K] . [W_vocab; W_store]^T
+// (bf16 in, float32 accumulate).  The first V columns are reduced on the fly to per-row
+// top-KP lists over each CTA's column slice, pval/pid [R, n_split, KP] (value desc, id
+// asc; *n_split_out receives n_split); the next n_store columns (W_store rows) are stored
+// as float32 out[r * ldo + n].  V = 0 or n_store = 0 drops that segment.
+cudaError_t launch_lm_head(const void *hidden, int R, int K, const void *W_vocab, int V, int KP, float *pval,
+                           int32_t *pid, int *n_split_out, const void *W_store, int n_store, float *out,
+                           long long ldo, uint32_t *status, cudaStream_t stream);
 
-// Same product stored as float32: out[r * ldo + n].
+// C = A[R, K] . B[N, K]^T stored as float32 out[r * ldo + n] (the store segment alone).
 cudaError_t launch_gemm_store(const void *A, const void *B, int R, int K, int N, float *out, long long ldo,
                               uint32_t *status, cudaStream_t stream);
 
@@ -34,6 +37,15 @@ cudaError_t launch_logits_topk_partial(const float *logits, int R, int V, int KP
 // Merge [R, n_split, KP] partial lists into the top-k of each row (value desc, id asc).
 cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int n_split, int KP, int k,
                               int32_t *topk_ids, float *topk_vals, cudaStream_t stream);
+
+// Everything after the lists in one launch (programmatic dependent launch): merge of
+// the [R, n_split, KP] lists, lattice rows, and the walk by the last CTA of each
+// sequence (best [R, k] is scratch for the walk's choices).  counters [B] must be zero
+// before the call and are zero after it.
+cudaError_t launch_finish(int B, int T, int k, int V, int D, int KP, int n_split, const float *pval,
+                          const int32_t *pid, const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
+                          const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
+                          float *topk_vals, int32_t *best, unsigned *counters, cudaStream_t stream);
 
 // Packed lattice rows [B*T, k + k*k] from candidates, unary scores, gate and codebooks.
 cudaError_t launch_lattice(int B, int T, int k, int V, int D, const int32_t *topk_ids, const float *topk_vals,

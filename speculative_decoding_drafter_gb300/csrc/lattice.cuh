@@ -1,0 +1,203 @@
+// lattice.cuh -- device steps shared by the fused finish kernel and the stage kernels:
+// one draft position's row of the k x k transition lattice, and the greedy walk.
+//
+// "DFlash 2: Keep Drafting Parallel", section "A Lightweight Path Selector":
+//   S_t(a, b) = U_t(b) + < A(a) (.) H(h_t), B(b) >
+// with a among the previous position's candidates (the last verified token at the
+// first position) and b among the current ones; greedy follows the best successor from
+// the last verified token.  "DFlash2 Lands in llama.cpp", sections "The Central
+// Insight" (edge = unary + pairwise) and "What llama.cpp Actually Builds for the
+// Selector" (codebook gathers, rows packed as candidate ids followed by transition
+// scores, walk with predecessor = anchor).
+#pragma once
+
+#include <cstdint>
+
+#include "topk.cuh"
+
+namespace df2 {
+
+constexpr int kLatticeThreads = 256;
+
+__device__ __forceinline__ int clamp_id(int id, int V)
+{
+    return static_cast<unsigned>(id) < static_cast<unsigned>(V) ? id : 0;
+}
+
+// Dynamic shared memory of one lattice row: the gate row as float [D], then the gathered
+// codebook rows as bf16: up to k predecessor rows A(prev_i) followed by k rows B(cand_j).
+__host__ __device__ constexpr size_t lattice_smem_bytes(int k, int D)
+{
+    return sizeof(float) * static_cast<size_t>(D) + sizeof(uint16_t) * 2 * static_cast<size_t>(k) * D;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Copies the gate row g[0..D) into shared memory (threads [first, first + count) of the CTA).
+__device__ __forceinline__ void load_gate_row(float *sg, const float *__restrict__ g, int D, int first, int count)
+{
+    for (int i = threadIdx.x - first; i >= 0 && i < D / 4; i += count)
+        reinterpret_cast<float4 *>(sg)[i] = reinterpret_cast<const float4 *>(g)[i];
+}
+
+// Sum of v[j] over the 32 lanes, left in lane j for j < KP (KP a power of two <= 32):
+// a reduce-scatter butterfly, KP - 1 + log2(32 / KP) shuffles instead of 5 * KP.
+template <int KP>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[KP])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = KP / 2; h >= 1; h >>= 1) {
+        const bool upper = (lane & h) != 0;
+#pragma unroll
+        for (int q = 0; q < h; ++q) {
+            const float send = upper ? v[q] : v[q + h];
+            const float keep = upper ? v[q + h] : v[q];
+            v[q] = keep + __shfl_xor_sync(kFullMask, send, h);
+        }
+    }
+    float x = v[0];
+#pragma unroll
+    for (int o = KP; o < 32; o <<= 1)
+        x += __shfl_xor_sync(kFullMask, x, o);
+    return x;  // lane l holds the total of index l & (KP - 1)
+}
+
+// Writes packed row r of the lattice: [cand ids | unary_j + <A(prev_i) (.) g, B(cand_j)>].
+// prev[0..n_prev) are the predecessor tokens (n_prev = 1 at t = 0: the anchor, whose
+// scores are copied to all k predecessor rows), cand/unary the current candidates, and
+// sg the gate row, already in shared memory at the start of `smem`.
+// If `best` is not null, best[i] receives the walk's choice from predecessor row i:
+// the index of the row's maximum, lowest index on ties.
+// All CTA threads call it; it starts and ends with __syncthreads().
+template <int KP>
+__device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const int *s_cand, const float *s_unary,
+                            const uint16_t *__restrict__ pred_cb, const uint16_t *__restrict__ succ_cb,
+                            uint8_t *smem, float *__restrict__ out, int32_t *__restrict__ best = nullptr)
+{
+    constexpr int kBatch = 8;  // 16-byte gathers in flight per thread
+    const float *sg = reinterpret_cast<const float *>(smem);                  // [D] gate
+    uint16_t *rows = reinterpret_cast<uint16_t *>(smem + sizeof(float) * D);  // [n_prev + k][D]
+    __syncthreads();
+    const int chunks = D / 8;  // 16-byte chunks of bf16 per codebook row
+    const int total = (n_prev + k) * chunks;
+    for (int base = threadIdx.x; base < total; base += blockDim.x * kBatch) {
+        uint4 w[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int idx = base + q * blockDim.x;
+            if (idx < total) {
+                const int row = idx / chunks;
+                const int c8 = idx - row * chunks;
+                const uint16_t *src = row < n_prev ? pred_cb + static_cast<long long>(s_prev[row]) * D
+                                                   : succ_cb + static_cast<long long>(s_cand[row - n_prev]) * D;
+                w[q] = __ldg(reinterpret_cast<const uint4 *>(src) + c8);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+            const int idx = base + q * blockDim.x;
+            if (idx < total)
+                reinterpret_cast<uint4 *>(rows)[idx] = w[q];
+        }
+    }
+    __syncthreads();
+
+    // Each warp takes two predecessor rows at a time; lanes stride over pairs of d.
+    const uint32_t *succ2 = reinterpret_cast<const uint32_t *>(rows + n_prev * D);  // [k][D/2]
+    const float2 *g2 = reinterpret_cast<const float2 *>(sg);
+    const int D2 = D / 2;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_warps = blockDim.x >> 5;
+    for (int i0 = 2 * warp; i0 < n_prev; i0 += 2 * n_warps) {
+        const bool two = i0 + 1 < n_prev;
+        const uint32_t *a0 = reinterpret_cast<const uint32_t *>(rows + i0 * D);
+        const uint32_t *a1 = two ? a0 + D2 : a0;
+        float acc0[KP], acc1[KP];
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            acc0[j] = 0.f;
+            acc1[j] = 0.f;
+        }
+        for (int d2 = lane; d2 < D2; d2 += 32) {
+            const float2 gg = g2[d2];
+            const uint32_t p0 = a0[d2], p1 = a1[d2];
+            const float x0 = bf16_lo(p0) * gg.x, y0 = bf16_hi(p0) * gg.y;  // A(prev) (.) g
+            const float x1 = bf16_lo(p1) * gg.x, y1 = bf16_hi(p1) * gg.y;
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                if (j < k) {
+                    const uint32_t sb = succ2[j * D2 + d2];
+                    const float sl = bf16_lo(sb), sh = bf16_hi(sb);
+                    acc0[j] = fmaf(y0, sh, fmaf(x0, sl, acc0[j]));
+                    acc1[j] = fmaf(y1, sh, fmaf(x1, sl, acc1[j]));
+                }
+            }
+        }
+        const float tot0 = warp_reduce_scatter<KP>(acc0);
+        const float tot1 = warp_reduce_scatter<KP>(acc1);
+        for (int h = 0; h < (two ? 2 : 1); ++h) {
+            const int i = i0 + h;
+            const float s = lane < k ? s_unary[lane] + (h == 0 ? tot0 : tot1) : -INFINITY;
+            if (lane < k) {
+                if (n_prev == 1) {
+                    for (int ii = 0; ii < k; ++ii)
+                        out[k + ii * k + lane] = s;
+                } else {
+                    out[k + i * k + lane] = s;
+                }
+            }
+            if (best) {
+                float x = s;
+                int j = lane < k ? lane : 0x7fffffff;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float ox = __shfl_xor_sync(kFullMask, x, off);
+                    const int oj = __shfl_xor_sync(kFullMask, j, off);
+                    const bool take = ranks_before(ox, oj, x, j);
+                    x = take ? ox : x;
+                    j = take ? oj : j;
+                }
+                if (lane == 0)
+                    best[i] = j;
+            }
+        }
+    }
+    if (threadIdx.x < k)
+        out[threadIdx.x] = static_cast<float>(s_cand[threadIdx.x]);
+    __syncthreads();
+}
+
+// Greedy walk of one sequence by one warp over its T packed rows (row stride `width`
+// floats): j_0 = argmax of predecessor row 0 at t = 0, then j_t = argmax of row
+// j_(t-1); ties go to the lowest candidate index.  kGlobal reads through L2 (rows
+// written by other CTAs of the same grid); otherwise `rows` is in shared memory.
+template <bool kGlobal>
+__device__ __forceinline__ void walk_rows(int T, int k, long long width, const float *rows, int32_t *draft)
+{
+    const int lane = threadIdx.x & 31;
+    int jp = 0;
+    for (int t = 0; t < T; ++t) {
+        const float *row = rows + static_cast<long long>(t) * width;
+        const float *p = row + k + jp * k + lane;
+        float x = -INFINITY;
+        if (lane < k)
+            x = kGlobal ? __ldcg(p) : *p;
+        int j = lane < k ? lane : 0x7fffffff;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ox = __shfl_xor_sync(kFullMask, x, off);
+            const int oj = __shfl_xor_sync(kFullMask, j, off);
+            const bool take = ranks_before(ox, oj, x, j);
+            x = take ? ox : x;
+            j = take ? oj : j;
+        }
+        jp = j;
+        if (lane == 0)
+            draft[t] = static_cast<int32_t>(kGlobal ? __ldcg(row + jp) : row[jp]);
+    }
+}
+
+}  // namespace df2

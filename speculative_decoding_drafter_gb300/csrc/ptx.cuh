@@ -82,6 +82,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Lets the next kernel in the stream (launched with programmatic stream serialisation)
+// start its prologue; its griddep_wait() still waits for this grid to finish.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the grids this one depends on have completed and their writes are visible
+// (returns at once when the kernel was launched without the dependency attribute).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)

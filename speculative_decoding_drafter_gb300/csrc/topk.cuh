@@ -13,9 +13,11 @@ namespace df2 {
 
 constexpr unsigned kFullMask = 0xffffffffu;
 
+// Branch-free (no short-circuit): the sorting networks below evaluate it thousands of
+// times per warp, and a branch per comparison costs more than the comparison.
 __device__ __forceinline__ bool ranks_before(float va, int ia, float vb, int ib)
 {
-    return va > vb || (va == vb && ia < ib);
+    return (va > vb) | ((va == vb) & (ia < ib));
 }
 
 // Sorted per-thread list of KP (value, id) pairs held in registers.
@@ -56,7 +58,75 @@ struct ThreadTopK {
             i[0] = id;
         }
     }
+
+    // Insert under the full order (value desc, id asc), ids in any order.
+    __device__ __forceinline__ void push(float x, int id)
+    {
+        if (!ranks_before(x, id, v[KP - 1], i[KP - 1]))
+            return;
+#pragma unroll
+        for (int s = KP - 1; s > 0; --s) {
+            if (ranks_before(x, id, v[s - 1], i[s - 1])) {
+                v[s] = v[s - 1];
+                i[s] = i[s - 1];
+            } else if (ranks_before(x, id, v[s], i[s])) {
+                v[s] = x;
+                i[s] = id;
+            }
+        }
+        if (ranks_before(x, id, v[0], i[0])) {
+            v[0] = x;
+            i[0] = id;
+        }
+    }
 };
+
+// Top-KP of two lists sorted by (value desc, id asc), kept in a: the elementwise better
+// of a[i] and b[KP-1-i] is a bitonic sequence holding exactly the KP best of the union,
+// and a bitonic merge network sorts it again.  Fixed cost, no data-dependent branches.
+template <int KP>
+__device__ __forceinline__ void merge_top(float (&av)[KP], int (&ai)[KP], const float (&bv)[KP], const int (&bi)[KP])
+{
+#pragma unroll
+    for (int s = 0; s < KP; ++s) {
+        const bool take = ranks_before(bv[KP - 1 - s], bi[KP - 1 - s], av[s], ai[s]);
+        av[s] = take ? bv[KP - 1 - s] : av[s];
+        ai[s] = take ? bi[KP - 1 - s] : ai[s];
+    }
+#pragma unroll
+    for (int stride = KP / 2; stride > 0; stride >>= 1) {
+#pragma unroll
+        for (int s = 0; s < KP; ++s) {
+            if ((s & stride) == 0) {
+                const int t = s + stride;
+                const bool sw = ranks_before(av[t], ai[t], av[s], ai[s]);
+                const float tv = av[s];
+                const int ti = ai[s];
+                av[s] = sw ? av[t] : av[s];
+                ai[s] = sw ? ai[t] : ai[s];
+                av[t] = sw ? tv : av[t];
+                ai[t] = sw ? ti : ai[t];
+            }
+        }
+    }
+}
+
+// Butterfly over the lanes whose index differs in the bits of `lane_mask` (a power of two
+// minus one): afterwards each lane holds the top-KP of the lists of its group.
+template <int KP>
+__device__ __forceinline__ void warp_merge_top(float (&av)[KP], int (&ai)[KP], int lane_mask)
+{
+    for (int stride = 1; stride <= lane_mask; stride <<= 1) {
+        float bv[KP];
+        int bi[KP];
+#pragma unroll
+        for (int s = 0; s < KP; ++s) {
+            bv[s] = __shfl_xor_sync(kFullMask, av[s], stride);
+            bi[s] = __shfl_xor_sync(kFullMask, ai[s], stride);
+        }
+        merge_top<KP>(av, ai, bv, bi);
+    }
+}
 
 // Warp-wide sorted list: lane j holds entry j (32 slots, only the first k are used by
 // the callers; the rest are valid lower-ranked entries or sentinels).

@@ -65,7 +65,7 @@ def library(path: str | None = None):
             D = ctypes.POINTER(Dims)
             sig = {
                 "dflash2_workspace_bytes": (S, [D]),
-                "dflash2_workspace_init": (I, [P, S, P]),
+                "dflash2_workspace_init": (I, [D, P, S, P]),
                 "dflash2_select": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "dflash2_select_from_logits": (I, [D, P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "dflash2_lm_head_logits": (I, [D, P, P, P, P, S, P]),
@@ -136,13 +136,14 @@ def dflash2_workspace_bytes(dims: Dims) -> int:
     return int(library().dflash2_workspace_bytes(ctypes.byref(dims)))
 
 
-def dflash2_workspace_init(workspace: torch.Tensor, stream=None) -> None:
-    _check(library().dflash2_workspace_init(workspace.data_ptr(), workspace.numel(), _stream(stream)),
-           "dflash2_workspace_init")
+def dflash2_workspace_init(workspace: "Workspace", stream=None) -> None:
+    """Zero the workspace's control block (status word, per-sequence counters) on the stream."""
+    _check(library().dflash2_workspace_init(ctypes.byref(workspace.dims), workspace.ptr, workspace.nbytes,
+                                            _stream(stream)), "dflash2_workspace_init")
 
 
 class Workspace:
-    """Device scratch for one problem size (uint8 tensor, 256-byte aligned, status word zeroed)."""
+    """Device scratch for one problem size (uint8 tensor, 256-byte aligned, allocated zeroed)."""
 
     def __init__(self, dims: Dims, device=None):
         n = dflash2_workspace_bytes(dims)

@@ -57,7 +57,7 @@ def test_workspace_bytes_and_dimension_limits(lib):
 
     n = dflash2_workspace_bytes(dims())
     R, kp = 16, 8
-    assert n >= 256 + R * 256 * kp * 8 + R * 8 * 8 + R * 256 * 4
+    assert n >= 256 + 256 + R * 256 * kp * 8 + R * 8 * 4 + R * 256 * 4
     assert n % 256 == 0
     for bad in (dims(k=0), dims(k=33), dims(V=4, k=8), dims(H=4100), dims(D=12), dims(D=2048), dims(B=0),
                 dims(T=0), dims(V=1 << 24), dims(B=1 << 16, T=32)):
@@ -97,4 +97,6 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     assert lib.dflash2_lm_head_logits(ctypes.byref(d), 0x1008, 0x2000, 0x3000, 0x100000, 1 << 40,
                                       None) == DF2_ERR_INVALID_ARG
     assert lib.dflash2_check_device_status(None, 0, None) == DF2_ERR_WORKSPACE
-    assert lib.dflash2_workspace_init(0x100010, 4096, None) == DF2_ERR_WORKSPACE
+    assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100010, 1 << 40, None) == DF2_ERR_WORKSPACE
+    assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100000, 4096, None) == DF2_ERR_WORKSPACE
+    assert lib.dflash2_workspace_init(ctypes.byref(dims(k=0)), 0x100000, 1 << 40, None) == DF2_ERR_INVALID_ARG
