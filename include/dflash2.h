@@ -171,6 +171,22 @@ DF2_API df2_status dflash2_lattice(const df2_dims *dims, const int32_t *topk_ids
 /* Walk alone over packed rows: one warp per sequence; ties go to the lowest candidate index. */
 DF2_API df2_status dflash2_walk(const df2_dims *dims, const float *lattice, int32_t *draft_ids, void *stream);
 
+/* Walk with confidence, p_min early stop and optional sampling, over packed rows (the
+ * lattice dflash2_select writes).  On the row the walk reads, p = softmax(S / temperature).
+ * uniforms == NULL: greedy (first maximum, as dflash2_walk).  Otherwise uniforms float
+ * [B, T] in [0, 1): position t takes the first candidate whose running sum of p (in
+ * candidate order) exceeds uniforms[b, t] -- the draw comes from the same scores ("DFlash 2:
+ * Keep Drafting Parallel", section "A Lightweight Path Selector"); the caller supplies the
+ * random numbers.  The chosen transition's p is its confidence; when it is below p_min the
+ * walk stops ("DFlash2 Lands in llama.cpp", section "p_min Means Something Different Under
+ * DFlash2"): draft_ids is -1 from that position on and n_draft[b] (optional) counts the
+ * tokens emitted.  confidence float [B, T] (optional) holds p up to and including the stop,
+ * 0 after.  temperature must be finite and > 0; p_min <= 0 never stops.  Probabilities are
+ * float32 with expf. */
+DF2_API df2_status dflash2_walk_sample(const df2_dims *dims, const float *lattice, float temperature, float p_min,
+                                       const float *uniforms, int32_t *draft_ids, int32_t *n_draft,
+                                       float *confidence, void *stream);
+
 /* Synchronises `stream`, reads and clears the sticky device status word in `workspace`.
  * Returns DF2_ERR_TIMEOUT if a pipeline wait inside any kernel gave up since the last
  * check (the kernel then skipped its remaining work and its outputs are invalid). */

@@ -17,6 +17,10 @@ step cites the passage it follows in ``oracle.c``'s header:
   [k ids | k*k scores, predecessor-major]; the anchor is the predecessor at
   position 0.
 * ``walk``    -- greedy walk from the anchor, first maximum wins.
+* ``walk_sample`` -- the walk with the chosen transition's softmax confidence,
+  the p_min early stop ("DFlash2 Lands in llama.cpp", section "p_min Means
+  Something Different Under DFlash2") and inverse-CDF sampling from the same
+  scores with given uniforms (DFlash 2 page, "A Lightweight Path Selector").
 * ``select`` / ``select_from_logits`` -- the whole path for a set of
   sequences.
 """
@@ -66,8 +70,9 @@ def _load():
         lib.oracle_lattice.argtypes = [i64, i64, i32, i64, i64, p, p, p, p, p, p, p, p]
         lib.oracle_walk.argtypes = [i64, i64, i32, p, p, p]
         lib.oracle_threads.argtypes = []
+        lib.oracle_walk_sample.argtypes = [i64, i64, i32, p, ctypes.c_double, ctypes.c_double, p, p, p, p]
         for f in (lib.oracle_logits, lib.oracle_topk, lib.oracle_gate, lib.oracle_lattice, lib.oracle_walk,
-                  lib.oracle_threads):
+                  lib.oracle_threads, lib.oracle_walk_sample):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -154,6 +159,23 @@ def walk(lattice_f32, B: int, T: int, k: int):
     choice = np.empty((B, T), np.int32)
     _check(lib.oracle_walk(B, T, k, _ptr(lat), _ptr(draft), _ptr(choice)), "walk")
     return draft, choice
+
+
+def walk_sample(lattice_f32, B: int, T: int, k: int, temperature: float = 1.0, p_min: float = 0.0, uniforms=None):
+    """Walk with confidence and p_min stop; sampling when ``uniforms`` [B, T] is given.
+
+    Returns (draft int32 [B, T] with -1 after a stop, n_draft int32 [B], confidence float64 [B, T]).
+    """
+    lib = _load()
+    lat = _c(lattice_f32, np.float32)
+    assert lat.shape == (B * T, k + k * k)
+    u = None if uniforms is None else _c(uniforms, np.float32).reshape(B * T)
+    draft = np.empty((B, T), np.int32)
+    n = np.empty(B, np.int32)
+    conf = np.empty((B, T), np.float64)
+    _check(lib.oracle_walk_sample(B, T, k, _ptr(lat), float(temperature), float(p_min), _ptr(u), _ptr(draft), _ptr(n),
+                                  _ptr(conf)), "walk_sample")
+    return draft, n, conf
 
 
 def walk_margins(lattice64, choice):

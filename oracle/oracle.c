@@ -38,6 +38,14 @@
  *     draft[b,t] = cand[(b,t), j_t]; the first maximum wins (llama.cpp page,
  *     the predecessor = anchor walk; DFlash 2 page: greedy follows the best
  *     successor at each step).  Decided on the float32 lattice.
+ *  7. Confidence, p_min and sampling (oracle_walk_sample).  On the row the
+ *     walk reads, p_j = softmax(S / temperature)_j.  Greedy takes the first
+ *     maximum; sampling takes the first j whose running sum of p (in index
+ *     order) exceeds the given uniform u (DFlash 2 page: sampling draws from
+ *     the same scores).  The chosen transition's confidence is p_{j_t}; when it
+ *     is below p_min the walk stops and emits nothing from t on ("DFlash2 Lands
+ *     in llama.cpp", section "p_min Means Something Different Under DFlash2").
+ *     Computed in double.
  *
  * bf16 tensors are passed as their uint16 bit patterns.  Every function
  * returns 0 on success and a negative code on bad arguments or non-finite
@@ -221,5 +229,79 @@ int oracle_walk(int64_t B, int64_t T, int32_t k, const float *lattice, int32_t *
             jprev = best;
         }
     }
+    return 0;
+}
+
+/*
+ * Step 7: walk with confidence, p_min early stop and optional sampling on the
+ * packed float32 lattice.  uniforms [B*T] in [0,1) selects sampling (NULL:
+ * greedy).  Outputs draft [B*T] (-1 from the stop on), n_draft [B] (tokens
+ * emitted), confidence [B*T] (p of the chosen transition up to and including
+ * the stopping step, 0 after it).  temperature must be > 0.
+ */
+int oracle_walk_sample(int64_t B, int64_t T, int32_t k, const float *lattice, double temperature, double p_min,
+                       const float *uniforms, int32_t *draft, int32_t *n_draft, double *confidence)
+{
+    if (B < 0 || T <= 0 || k < 1 || !lattice || !draft || !n_draft || !confidence || !(temperature > 0.0))
+        return -1;
+    const int64_t width = (int64_t)k + (int64_t)k * k;
+    double *p = (double *)malloc((size_t)k * sizeof *p);
+    if (!p)
+        return -3;
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t jprev = 0;
+        int stopped = 0;
+        n_draft[b] = (int32_t)T;
+        for (int64_t t = 0; t < T; ++t) {
+            const int64_t r = b * T + t;
+            if (stopped) {
+                draft[r] = -1;
+                confidence[r] = 0.0;
+                continue;
+            }
+            const float *row = lattice + r * width;
+            const float *scores = row + k + (int64_t)jprev * k;
+            double m = scores[0];
+            for (int32_t j = 1; j < k; ++j)
+                if (scores[j] > m)
+                    m = scores[j];
+            double z = 0.0;
+            for (int32_t j = 0; j < k; ++j) {
+                p[j] = exp(((double)scores[j] - m) / temperature);
+                z += p[j];
+            }
+            for (int32_t j = 0; j < k; ++j)
+                p[j] /= z;
+            int32_t pick = 0;
+            if (uniforms) {
+                const double u = uniforms[r];
+                double run = 0.0;
+                pick = k - 1; /* if rounding leaves the total at or below u: the last candidate with weight */
+                while (pick > 0 && p[pick] == 0.0)
+                    --pick;
+                for (int32_t j = 0; j < k; ++j) {
+                    run += p[j];
+                    if (run > u) {
+                        pick = j;
+                        break;
+                    }
+                }
+            } else {
+                for (int32_t j = 1; j < k; ++j)
+                    if (scores[j] > scores[pick])
+                        pick = j;
+            }
+            confidence[r] = p[pick];
+            if (p[pick] < p_min) {
+                stopped = 1;
+                n_draft[b] = (int32_t)t;
+                draft[r] = -1;
+                continue;
+            }
+            draft[r] = (int32_t)row[pick];
+            jprev = pick;
+        }
+    }
+    free(p);
     return 0;
 }

@@ -3,6 +3,7 @@
 // (except dflash2_check_device_status).
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -289,6 +290,24 @@ df2_status dflash2_walk(const df2_dims *dims, const float *lattice, int32_t *dra
         return DF2_ERR_INVALID_ARG;
     cudaGetLastError();
     DF2_CUDA(launch_walk(d.B, d.T, d.k, lattice, draft_ids, static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
+df2_status dflash2_walk_sample(const df2_dims *dims, const float *lattice, float temperature, float p_min,
+                               const float *uniforms, int32_t *draft_ids, int32_t *n_draft, float *confidence,
+                               void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!lattice || !draft_ids || !aligned(lattice, 4) || !aligned(draft_ids, 4) ||
+        (uniforms && !aligned(uniforms, 4)) || (n_draft && !aligned(n_draft, 4)) ||
+        (confidence && !aligned(confidence, 4)))
+        return DF2_ERR_INVALID_ARG;
+    if (!(temperature > 0.f) || !std::isfinite(temperature) || std::isnan(p_min))
+        return DF2_ERR_INVALID_ARG;
+    cudaGetLastError();
+    DF2_CUDA(launch_walk_sample(d.B, d.T, d.k, lattice, temperature, p_min, uniforms, draft_ids, n_draft, confidence,
+                                static_cast<cudaStream_t>(stream)));
     return DF2_OK;
 }
 

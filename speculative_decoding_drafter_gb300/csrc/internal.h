@@ -52,6 +52,11 @@ cudaError_t launch_lattice(int B, int T, int k, int V, int D, const int32_t *top
                            const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
                            const int32_t *anchor, float *lattice, cudaStream_t stream);
 
+// Walk with confidence, p_min stop and optional sampling (uniforms [B*T] or null).
+cudaError_t launch_walk_sample(int B, int T, int k, const float *lattice, float temperature, float p_min,
+                               const float *uniforms, int32_t *draft_ids, int32_t *n_draft, float *confidence,
+                               cudaStream_t stream);
+
 // Greedy walk, one warp per sequence: draft_ids [B, T].
 cudaError_t launch_walk(int B, int T, int k, const float *lattice, int32_t *draft_ids, cudaStream_t stream);
 

@@ -21,7 +21,7 @@ __all__ = [
     "DFlash2Error", "Dims", "library", "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select",
     "dflash2_select_from_logits", "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice",
     "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
-    "dflash2_profile_events", "dflash2_topk_noalloc",
+    "dflash2_profile_events", "dflash2_topk_noalloc", "dflash2_walk_sample",
     "EXPORTED_SYMBOLS",
 ]
 
@@ -29,7 +29,7 @@ EXPORTED_SYMBOLS = (
     "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select", "dflash2_select_from_logits",
     "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
     "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
-    "dflash2_topk_noalloc",
+    "dflash2_topk_noalloc", "dflash2_walk_sample",
 )
 
 
@@ -78,6 +78,7 @@ def library(path: str | None = None):
                 "dflash2_version": (ctypes.c_int32, []),
                 "dflash2_profile_events": (I, [P, P]),
                 "dflash2_topk_noalloc": (I, [D, P, P, P, P]),
+                "dflash2_walk_sample": (I, [D, P, ctypes.c_float, ctypes.c_float, P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -306,6 +307,26 @@ def dflash2_walk(lattice, B: int, T: int, k: int, *, out=None, stream=None):
                                 _ptr(out, torch.int32, (B, T), "draft_ids"), _stream(stream))
     _check(st, "dflash2_walk")
     return out
+
+
+def dflash2_walk_sample(lattice, B: int, T: int, k: int, *, temperature: float = 1.0, p_min: float = 0.0,
+                        uniforms=None, draft=None, n_draft=None, confidence=None, stream=None):
+    """Walk with confidence and p_min stop; inverse-CDF sampling when ``uniforms`` [B, T] is given.
+
+    Returns (draft int32 [B, T] with -1 from a stop on, n_draft int32 [B], confidence float32 [B, T])."""
+    d = make_dims(B, T, 8, max(k, 1), k, 8)
+    dev = lattice.device
+    draft = draft if draft is not None else torch.empty((B, T), dtype=torch.int32, device=dev)
+    n_draft = n_draft if n_draft is not None else torch.empty((B,), dtype=torch.int32, device=dev)
+    confidence = confidence if confidence is not None else torch.empty((B, T), dtype=torch.float32, device=dev)
+    st = library().dflash2_walk_sample(ctypes.byref(d), _ptr(lattice, torch.float32, (B * T, k + k * k), "lattice"),
+                                       float(temperature), float(p_min),
+                                       _ptr(uniforms, torch.float32, (B, T), "uniforms"),
+                                       _ptr(draft, torch.int32, (B, T), "draft_ids"),
+                                       _ptr(n_draft, torch.int32, (B,), "n_draft"),
+                                       _ptr(confidence, torch.float32, (B, T), "confidence"), _stream(stream))
+    _check(st, "dflash2_walk_sample")
+    return draft, n_draft, confidence
 
 
 def dflash2_check_device_status(workspace: Workspace, stream=None) -> None:

@@ -97,6 +97,14 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     assert lib.dflash2_lm_head_logits(ctypes.byref(d), 0x1008, 0x2000, 0x3000, 0x100000, 1 << 40,
                                       None) == DF2_ERR_INVALID_ARG
     assert lib.dflash2_check_device_status(None, 0, None) == DF2_ERR_WORKSPACE
+    assert lib.dflash2_walk_sample(ctypes.byref(d), 0x1000, 0.0, 0.5, None, 0x2000, None, None,
+                                   None) == DF2_ERR_INVALID_ARG  # temperature must be > 0
+    assert lib.dflash2_walk_sample(ctypes.byref(d), 0x1000, float("inf"), 0.5, None, 0x2000, None, None,
+                                   None) == DF2_ERR_INVALID_ARG
+    assert lib.dflash2_walk_sample(ctypes.byref(d), 0x1000, 1.0, float("nan"), None, 0x2000, None, None,
+                                   None) == DF2_ERR_INVALID_ARG
+    assert lib.dflash2_walk_sample(ctypes.byref(d), None, 1.0, 0.5, None, 0x2000, None, None,
+                                   None) == DF2_ERR_INVALID_ARG
     assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100010, 1 << 40, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100000, 4096, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_workspace_init(ctypes.byref(dims(k=0)), 0x100000, 1 << 40, None) == DF2_ERR_INVALID_ARG

@@ -270,3 +270,65 @@ def test_k1_walk_is_top1():
     for r in range(15):
         g = int(lat[r, 0])
         assert ora["logits"][r, g] >= ora["topk_vals"][r, 0] - tol[r]
+
+
+# ---------------------------------------------------------------- confidence, p_min and sampling
+
+
+def _softmax64(row, tau):
+    z = (row.astype(np.float64) - row.max()) / tau
+    e = np.exp(z)
+    return e / e.sum()
+
+
+@pytest.mark.parametrize("B,T,k,tau,p_min", [(5, 16, 8, 1.0, 0.0), (4, 16, 16, 0.7, 0.2), (3, 9, 32, 1.3, 0.05),
+                                             (6, 8, 1, 1.0, 0.5), (64, 16, 16, 1.0, 0.3)])
+@pytest.mark.parametrize("sampling", [False, True])
+def test_walk_sample_stage(B, T, k, tau, p_min, sampling):
+    rng = np.random.default_rng(B * 100 + k + int(sampling))
+    lat = np.zeros((B * T, k + k * k), np.float32)
+    lat[:, :k] = rng.integers(0, 1 << 20, size=(B * T, k))
+    lat[:, k:] = (rng.standard_normal((B * T, k * k)) * 1.5).astype(np.float32)
+    for b in range(B):
+        lat[b * T, k:] = np.tile(lat[b * T, k:2 * k], k)
+    u = rng.random((B, T)).astype(np.float32) if sampling else None
+    d, n, c = df.dflash2_walk_sample(dev(lat), B, T, k, temperature=tau, p_min=p_min,
+                                     uniforms=None if u is None else dev(u))
+    d, n, c = host(d), host(n), host(c)
+    wd, wn, wc = oracle.walk_sample(lat, B, T, k, temperature=tau, p_min=p_min, uniforms=u)
+    eps = 1e-5
+    compared = 0
+    for b in range(B):
+        jp = 0
+        for t in range(T):
+            r = b * T + t
+            p = _softmax64(lat[r, k + jp * k: k + (jp + 1) * k], tau)
+            if sampling:
+                cut = np.abs(np.cumsum(p) - u[b, t]).min()
+                if cut <= eps:
+                    break
+            pick = int(np.where(lat[r, :k] == wd[b, t])[0][0]) if wd[b, t] >= 0 else None
+            conf = wc[b, t]
+            if abs(conf - p_min) <= eps:
+                break
+            assert abs(c[b, t] - conf) <= eps, (b, t)
+            assert d[b, t] == wd[b, t], (b, t)
+            compared += 1
+            if wd[b, t] < 0:  # both stopped here
+                assert n[b] == wn[b] == t and np.all(d[b, t:] == -1)
+                break
+            jp = pick
+        else:
+            assert n[b] == wn[b] == T
+    walked = int(np.minimum(wn + 1, T).sum())  # steps the oracle takes, the stopping step included
+    assert compared >= 0.8 * walked, (compared, walked)
+
+
+def test_walk_sample_greedy_reproduces_the_select_draft(case):
+    cfg = case["cfg"]
+    lat = torch.from_numpy(case["lat"]).cuda()
+    d, n, c = df.dflash2_walk_sample(lat, cfg.B, cfg.T, cfg.k, temperature=1.0, p_min=0.0)
+    assert np.array_equal(host(d), case["draft"])
+    assert np.all(host(n) == cfg.T)
+    conf = host(c)
+    assert np.all((conf > 0) & (conf <= 1.0 + 1e-6))

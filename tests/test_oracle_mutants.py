@@ -26,13 +26,21 @@ MUTANTS = {
                            "return (a->id > b->id) ? -1 : (a->id < b->id) ? 1 : 0;"),
     "walk_argmin": ("if (scores[j] > scores[best])", "if (scores[j] < scores[best])"),
     "walk_last_maximum": ("if (scores[j] > scores[best])", "if (scores[j] >= scores[best])"),
-    "walk_ignores_predecessor": ("const float *scores = row + k + (int64_t)jprev * k;",
-                                 "const float *scores = row + k;"),
+    "walk_ignores_predecessor": ("const float *scores = row + k + (int64_t)jprev * k;\n            int32_t best = 0;",
+                                 "const float *scores = row + k;\n            int32_t best = 0;"),
+    "sampled_walk_ignores_predecessor": ("const float *scores = row + k + (int64_t)jprev * k;\n            double m",
+                                         "const float *scores = row + k;\n            double m"),
     "logit_first_term_dropped": ("for (int64_t h = 0; h < H; ++h)\n                acc += bf16_to_double(hr[h])",
                                  "for (int64_t h = 1; h < H; ++h)\n                acc += bf16_to_double(hr[h])"),
     "logits_summed_in_float": ("            double acc = 0.0;\n            for (int64_t h = 0; h < H; ++h)\n                acc += bf16_to_double(hr[h])",
                                "            float acc = 0.0f;\n            for (int64_t h = 0; h < H; ++h)\n                acc += bf16_to_double(hr[h])"),
     "gate_transposed": ("bf16_to_double(W_sel[d * H + h])", "bf16_to_double(W_sel[h * D + d])"),
+    "confidence_of_the_maximum": ("            confidence[r] = p[pick];", "            confidence[r] = p[0] > p[pick] ? p[0] : p[pick];"),
+    "temperature_multiplies": ("p[j] = exp(((double)scores[j] - m) / temperature);",
+                               "p[j] = exp(((double)scores[j] - m) * temperature);"),
+    "stop_counts_the_low_step": ("                n_draft[b] = (int32_t)t;", "                n_draft[b] = (int32_t)t + 1;"),
+    "inverse_cdf_off_by_one": ("                    if (run > u) {\n                        pick = j;",
+                               "                    if (run > u) {\n                        pick = j + 1 < k ? j + 1 : j;"),
     "gate_of_wrong_row": ("bf16_to_double(hidden[r * H + h]);\n            gate[r * D + d] = acc;",
                           "bf16_to_double(hidden[(R - 1 - r) * H + h]);\n            gate[r * D + d] = acc;"),
 }

@@ -350,3 +350,89 @@ def test_sequences_are_block_local():
     out2 = oracle.select(hid[rows], W, Wsel, pred, succ, anchor[perm], k, T)
     assert np.array_equal(out2["draft"], out["draft"][perm])
     assert np.array_equal(out2["lattice"], out["lattice"][rows])
+
+
+# ---------------------------------------------------------------- step 7: confidence, p_min, sampling
+
+
+def _rows_lattice(scores_per_step, ids_per_step, k):
+    """One sequence whose every predecessor row at step t holds scores_per_step[t]."""
+    T = len(scores_per_step)
+    lat = np.zeros((T, k + k * k), np.float32)
+    for t in range(T):
+        lat[t, :k] = ids_per_step[t]
+        lat[t, k:] = np.tile(np.asarray(scores_per_step[t], np.float32), k)
+    return lat
+
+
+def test_greedy_confidence_of_two_candidates_is_the_logistic_function():
+    import math
+
+    for s0, s1, tau in ((1.5, 0.25, 1.0), (-2.0, 3.0, 0.5), (0.0, 0.0, 2.0)):
+        lat = _rows_lattice([[s0, s1]], [[7, 9]], 2)
+        draft, n, conf = oracle.walk_sample(lat, 1, 1, 2, temperature=tau)
+        pick = 0 if s0 >= s1 else 1
+        want = 1.0 / (1.0 + math.exp(-abs(np.float32(s0) - np.float32(s1)) / tau))
+        assert draft[0, 0] == [7, 9][pick]
+        assert conf[0, 0] == pytest.approx(want, rel=1e-12)
+        assert n[0] == 1
+
+
+def test_sampling_follows_the_inverse_cdf_of_a_designed_row():
+    # softmax(log p) = p: cumulative 0.1, 0.3, 0.6, 1.0
+    row = np.log(np.array([0.1, 0.2, 0.3, 0.4])).astype(np.float32)
+    for u, want in ((0.05, 0), (0.15, 1), (0.35, 2), (0.95, 3), (0.0, 0), (0.999, 3)):
+        lat = _rows_lattice([row], [[10, 11, 12, 13]], 4)
+        draft, n, conf = oracle.walk_sample(lat, 1, 1, 4, uniforms=np.array([[u]], np.float32))
+        assert draft[0, 0] == 10 + want, u
+
+
+def test_sampling_frequencies_match_the_softmax():
+    from scipy.special import softmax
+
+    rng = np.random.default_rng(31)
+    k, n_draws, tau = 6, 20000, 0.7
+    row = rng.standard_normal(k).astype(np.float32)
+    lat = np.tile(_rows_lattice([row], [np.arange(k)], k), (n_draws, 1))  # n_draws sequences of one step
+    u = rng.random((n_draws, 1)).astype(np.float32)
+    draft, n, conf = oracle.walk_sample(lat, n_draws, 1, k, temperature=tau, uniforms=u)
+    p = softmax(row.astype(np.float64) / tau)
+    freq = np.bincount(draft[:, 0], minlength=k) / n_draws
+    assert np.all(np.abs(freq - p) <= 4 * np.sqrt(p * (1 - p) / n_draws) + 1e-9)
+    assert np.allclose(conf[:, 0], p[draft[:, 0]])
+
+
+def test_p_min_stops_the_walk_where_confidence_first_drops():
+    k, T = 3, 5
+    sharp, flat = [4.0, 0.0, 0.0], [0.1, 0.0, 0.05]
+    steps = [sharp, sharp, sharp, flat, sharp]
+    lat = _rows_lattice(steps, [[100 + 10 * t + j for j in range(k)] for t in range(T)], k)
+    base, _ = oracle.walk(lat, 1, T, k)
+    draft, n, conf = oracle.walk_sample(lat, 1, T, k, p_min=0.5)
+    assert n[0] == 3
+    assert draft[0, :3].tolist() == base[0, :3].tolist()
+    assert draft[0, 3:].tolist() == [-1, -1]
+    assert conf[0, 3] < 0.5 and conf[0, 4] == 0.0
+    d0, n0, _ = oracle.walk_sample(lat, 1, T, k, p_min=0.0)
+    assert n0[0] == T and np.array_equal(d0, base)
+    d1, n1, _ = oracle.walk_sample(lat, 1, T, k, p_min=1.01)
+    assert n1[0] == 0 and np.all(d1 == -1)
+
+
+def test_sampling_at_vanishing_temperature_is_greedy_and_shift_invariant():
+    rng = np.random.default_rng(32)
+    B, T, k = 3, 6, 5
+    lat = np.zeros((B * T, k + k * k), np.float32)
+    lat[:, :k] = np.arange(B * T * k).reshape(B * T, k)
+    lat[:, k:] = (np.round(rng.standard_normal((B * T, k * k)) * 64) / 64).astype(np.float32)  # dyadic
+    for b in range(B):
+        lat[b * T, k:] = np.tile(lat[b * T, k:2 * k], k)
+    greedy, _ = oracle.walk(lat, B, T, k)
+    u = rng.random((B, T)).astype(np.float32)
+    cold, n, _ = oracle.walk_sample(lat, B, T, k, temperature=1e-6, uniforms=u)
+    assert np.array_equal(cold, greedy)
+    shifted = lat.copy()
+    shifted[:, k:] += np.float32(8.0)  # exact: the scores are multiples of 1/64 below 16
+    a = oracle.walk_sample(lat, B, T, k, temperature=0.9, uniforms=u)
+    b = oracle.walk_sample(shifted, B, T, k, temperature=0.9, uniforms=u)
+    assert np.array_equal(a[0], b[0]) and np.allclose(a[2], b[2], rtol=1e-12)
