@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="8b_b1", choices=list(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--op", default="select", choices=["select", "conv"],
+                    help="select: the selector head (default); conv: the dynamic local convolution")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     a = ap.parse_args()
@@ -375,11 +377,106 @@ def run_ours(args, cfg, rank: int, world: int):
     return 0
 
 
+CONV_SHAPE = (1024, 16, 4096, 16)  # blocks, positions per block, channels, channels per dynamic group
+
+
+def run_conv(args, rank: int, world: int):
+    """The dynamic local convolution (RMS-normalised input) on B=1024 blocks of 16 rows of 4096 channels."""
+    import torch
+
+    from speculative_decoding_drafter_gb300 import dflash2 as df
+    from speculative_decoding_drafter_gb300.synth import make_conv_inputs
+
+    if rank != 0 and args.impl == "reference":
+        return 0
+    B, T, C, G = CONV_SHAPE
+    c = make_conv_inputs(B, T, C, G, seed=0)
+    name = f"dynamic_conv: B={B} T={T} C={C} G={G}, RMS-normalised input"
+    peaks, peak_kind = load_peaks()
+    R = B * T
+    algo = R * C * 2 * 2 + B * C * 2 + R * 2 * (C // G) * 4 + 3 * C * 2  # x in, y out, x_prev, dyn, base+gamma
+    if args.impl == "reference":
+        import oracle
+
+        oracle.build()
+        rows = 64  # bounded sample: the first 4 blocks
+        t0 = time.perf_counter()
+        steps = 0
+        for _ in range(args.steps):
+            oracle.dynamic_conv(c["x"][:rows], c["x_prev"][:rows // T], c["base"], c["dyn"][:rows], T, G,
+                                gamma=c["gamma"], eps=1e-6)
+            steps += 1
+        dt = time.perf_counter() - t0
+        v = rows * steps / dt
+        print(json.dumps({"impl": "reference", "op": "conv", "metric": "dynamic conv rows/s", "value": v,
+                          "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * dt / steps, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": name},
+                          "cpu_baseline": {"value": v, "unit": "rows/s", "cores": oracle.threads(), "kind": "oracle",
+                                           "sample": f"{rows} rows per step"},
+                          "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+        return 0
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    x, xp, base, gm = dev_bf16(c["x"]), dev_bf16(c["x_prev"]), dev_bf16(c["base"]), dev_bf16(c["gamma"])
+    dyn = torch.from_numpy(c["dyn"]).cuda()
+    y = torch.empty_like(x)
+
+    def step():
+        df.dflash2_dynamic_conv(x, base, dyn, T, x_prev=xp, gamma=gm, eps=1e-6, G=G, out=y)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device_id_for_smi(torch)) if rank == 0 else None
+    if dist is not None:
+        dist.barrier()
+    if sampler:
+        sampler.start()
+    start.record()
+    for _ in range(args.steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clock_rows = sampler.stop() if sampler else []
+    ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
+    if rank == 0:
+        s_per = ms / args.steps / 1e3
+        achieved = algo / s_per / 1e9
+        print(json.dumps({
+            "impl": "ours", "op": "conv", "metric": "dynamic conv rows/s", "value": whole_job_rate(R, args.steps, world, ms),
+            "unit": "rows/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": name, "l2": f"x alone {R * C * 2 / 1e6:.0f} MB > 129 MB L2"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "dynamic_conv_kernel",
+                         "algorithmic_per_launch": algo, "peak_source": peak_kind},
+            "gpu_launches": args.steps,
+            "clocks": ClockSampler.summarize(clock_rows, 0) if clock_rows else {"reasons": ["no samples"]}}), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse_args()
     cfg = CONFIGS[args.config]
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    if args.op == "conv":
+        return run_conv(args, rank, world)
     if args.impl == "reference":
         return run_reference(args, cfg, rank)
     return run_ours(args, cfg, rank, world)

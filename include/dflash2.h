@@ -187,6 +187,32 @@ DF2_API df2_status dflash2_walk_sample(const df2_dims *dims, const float *lattic
                                        const float *uniforms, int32_t *draft_ids, int32_t *n_draft,
                                        float *confidence, void *stream);
 
+/* Dimensions of the dynamic local convolution: B blocks of T positions, C channels, G
+ * channels per dynamic group. */
+typedef struct df2_conv_dims {
+    int32_t B, T, C, G;
+} df2_conv_dims;
+
+/* Grouped two-tap dynamic depthwise convolution of the drafter's hidden states ("DFlash 2:
+ * Keep Drafting Parallel", section "A Lightweight Local Convolution": Conv_k(x)_t =
+ * k_{t,0} (.) x_t + k_{t,1} (.) x_{t-1}; "DFlash2 Lands in llama.cpp", section "Dynamic
+ * Local Convolution"):
+ *   y[r,c] = (base[0,c] + dyn[r,0,c/G]) * xn(x[r])[c] + (base[1,c] + dyn[r,1,c/G]) * xn(prev)[c]
+ * with prev = x[r-1] inside a block and x_prev[b] (the last verified token's row) at the
+ * first position; no row of another block is ever read.  xn is the identity, or with gamma
+ * the RMS normalisation v / sqrt(mean(v^2) + eps) * gamma (an all-zero row stays zero).
+ *   x      bf16 [B*T, C]      the block's hidden states (row b*T + t)
+ *   x_prev bf16 [B, C]        last verified token of each block, or NULL for a zero row
+ *   base   bf16 [2, C]        learned per-channel taps (0: the position, 1: its predecessor)
+ *   dyn    float [B*T, 2, C/G] per-group corrections, already projected from the hidden state
+ *   gamma  bf16 [C] or NULL   RMS-normalisation weight (NULL: no normalisation)
+ *   y      bf16 [B*T, C]      output (round to nearest even); must not overlap x or x_prev
+ * Limits: C % G == 0, G % 8 == 0, 8 <= C <= 8192, eps >= 0.  x, x_prev, base, gamma and y
+ * 16-byte aligned, dyn 4-byte aligned.  float32 arithmetic. */
+DF2_API df2_status dflash2_dynamic_conv(const df2_conv_dims *dims, const void *x, const void *x_prev,
+                                        const void *base, const float *dyn, const void *gamma, float eps, void *y,
+                                        void *stream);
+
 /* Synchronises `stream`, reads and clears the sticky device status word in `workspace`.
  * Returns DF2_ERR_TIMEOUT if a pipeline wait inside any kernel gave up since the last
  * check (the kernel then skipped its remaining work and its outputs are invalid). */

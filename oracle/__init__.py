@@ -21,6 +21,9 @@ step cites the passage it follows in ``oracle.c``'s header:
   the p_min early stop ("DFlash2 Lands in llama.cpp", section "p_min Means
   Something Different Under DFlash2") and inverse-CDF sampling from the same
   scores with given uniforms (DFlash 2 page, "A Lightweight Path Selector").
+* ``dynamic_conv`` -- grouped two-tap dynamic depthwise convolution ("DFlash 2:
+  Keep Drafting Parallel", section "A Lightweight Local Convolution"; "DFlash2
+  Lands in llama.cpp", section "Dynamic Local Convolution").
 * ``select`` / ``select_from_logits`` -- the whole path for a set of
   sequences.
 """
@@ -71,8 +74,9 @@ def _load():
         lib.oracle_walk.argtypes = [i64, i64, i32, p, p, p]
         lib.oracle_threads.argtypes = []
         lib.oracle_walk_sample.argtypes = [i64, i64, i32, p, ctypes.c_double, ctypes.c_double, p, p, p, p]
+        lib.oracle_dynamic_conv.argtypes = [i64, i64, i64, i64, p, p, p, p, p, ctypes.c_double, p]
         for f in (lib.oracle_logits, lib.oracle_topk, lib.oracle_gate, lib.oracle_lattice, lib.oracle_walk,
-                  lib.oracle_threads, lib.oracle_walk_sample):
+                  lib.oracle_threads, lib.oracle_walk_sample, lib.oracle_dynamic_conv):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -176,6 +180,28 @@ def walk_sample(lattice_f32, B: int, T: int, k: int, temperature: float = 1.0, p
     _check(lib.oracle_walk_sample(B, T, k, _ptr(lat), float(temperature), float(p_min), _ptr(u), _ptr(draft), _ptr(n),
                                   _ptr(conf)), "walk_sample")
     return draft, n, conf
+
+
+def dynamic_conv(x, x_prev, base, dyn, T: int, G: int = 16, gamma=None, eps: float = 1e-6):
+    """Two-tap dynamic depthwise conv over blocks of T rows, in double: y [B*T, C] float64.
+
+    x bf16 bits [B*T, C]; x_prev bf16 bits [B, C] or None (zeros); base bf16 bits [2, C]
+    (tap 0: the position itself, tap 1: its predecessor); dyn float32 [B*T, 2, C/G];
+    gamma bf16 bits [C] or None (no RMS normalisation)."""
+    lib = _load()
+    x = _c(x, np.uint16)
+    R, C = x.shape
+    B = R // T
+    assert B * T == R
+    xp = None if x_prev is None else _c(x_prev, np.uint16)
+    base = _c(base, np.uint16)
+    dyn = _c(dyn, np.float32)
+    gm = None if gamma is None else _c(gamma, np.uint16)
+    assert base.shape == (2, C) and dyn.shape == (R, 2, C // G)
+    y = np.empty((R, C), np.float64)
+    _check(lib.oracle_dynamic_conv(B, T, C, G, _ptr(x), _ptr(xp), _ptr(base), _ptr(dyn), _ptr(gm), float(eps),
+                                   _ptr(y)), "dynamic_conv")
+    return y
 
 
 def walk_margins(lattice64, choice):

@@ -305,3 +305,67 @@ int oracle_walk_sample(int64_t B, int64_t T, int32_t k, const float *lattice, do
     free(p);
     return 0;
 }
+
+/*
+ * Grouped two-tap dynamic depthwise convolution ("DFlash 2: Keep Drafting Parallel",
+ * section "A Lightweight Local Convolution": Conv_k(x)_t = k_{t,0} (.) x_t + k_{t,1} (.)
+ * x_{t-1}, each coefficient a learned base plus a correction shared by every 16
+ * channels, the first position reading the last verified token; "DFlash2 Lands in
+ * llama.cpp", section "Dynamic Local Convolution": static per-channel weight plus a
+ * per-group dynamic weight, block-local shift).  In double:
+ *   xn(v)   = v                                   without normalisation (gamma NULL)
+ *           = v / sqrt(mean(v^2) + eps) * gamma   RMS-normalised row (a zero row stays zero)
+ *   y[r,c]  = (base[0,c] + dyn[r,0,c/G]) * xn(x[r])[c] + (base[1,c] + dyn[r,1,c/G]) * xn(prev)[c]
+ *   prev    = x[r-1] for t > 0; x_prev[b] at t = 0 (a zero row if x_prev is NULL).
+ * x, x_prev, base, gamma: bf16 bits; dyn: float [B*T, 2, C/G]; y: double [B*T, C].
+ */
+int oracle_dynamic_conv(int64_t B, int64_t T, int64_t C, int64_t G, const uint16_t *x, const uint16_t *x_prev,
+                        const uint16_t *base, const float *dyn, const uint16_t *gamma, double eps, double *y)
+{
+    if (B < 0 || T <= 0 || C <= 0 || G <= 0 || C % G != 0 || !x || !base || !dyn || !y || eps < 0.0)
+        return -1;
+    const int64_t groups = C / G;
+    double *cur = (double *)malloc((size_t)C * sizeof *cur);
+    double *prv = (double *)malloc((size_t)C * sizeof *prv);
+    if (!cur || !prv) {
+        free(cur);
+        free(prv);
+        return -3;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t t = 0; t < T; ++t) {
+            const int64_t r = b * T + t;
+            for (int64_t c = 0; c < C; ++c) {
+                cur[c] = bf16_to_double(x[r * C + c]);
+                if (t > 0)
+                    prv[c] = bf16_to_double(x[(r - 1) * C + c]);
+                else
+                    prv[c] = x_prev ? bf16_to_double(x_prev[b * C + c]) : 0.0;
+            }
+            if (gamma) {
+                double sc = 0.0, sp = 0.0;
+                for (int64_t c = 0; c < C; ++c) {
+                    sc += cur[c] * cur[c];
+                    sp += prv[c] * prv[c];
+                }
+                /* an all-zero row normalises to zero (even with eps = 0) */
+                const double ic = (sc > 0.0 || eps > 0.0) ? 1.0 / sqrt(sc / (double)C + eps) : 0.0;
+                const double ip = (sp > 0.0 || eps > 0.0) ? 1.0 / sqrt(sp / (double)C + eps) : 0.0;
+                for (int64_t c = 0; c < C; ++c) {
+                    const double gm = bf16_to_double(gamma[c]);
+                    cur[c] = cur[c] * ic * gm;
+                    prv[c] = prv[c] * ip * gm;
+                }
+            }
+            for (int64_t c = 0; c < C; ++c) {
+                const int64_t g = c / G;
+                const double k0 = bf16_to_double(base[c]) + (double)dyn[(r * 2 + 0) * groups + g];
+                const double k1 = bf16_to_double(base[C + c]) + (double)dyn[(r * 2 + 1) * groups + g];
+                y[r * C + c] = k0 * cur[c] + k1 * prv[c];
+            }
+        }
+    }
+    free(cur);
+    free(prv);
+    return 0;
+}

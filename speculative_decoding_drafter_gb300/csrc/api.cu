@@ -311,6 +311,27 @@ df2_status dflash2_walk_sample(const df2_dims *dims, const float *lattice, float
     return DF2_OK;
 }
 
+df2_status dflash2_dynamic_conv(const df2_conv_dims *dims, const void *x, const void *x_prev, const void *base,
+                                const float *dyn, const void *gamma, float eps, void *y, void *stream)
+{
+    if (!dims)
+        return DF2_ERR_INVALID_ARG;
+    const df2_conv_dims d = *dims;
+    if (d.B < 1 || d.T < 1 || d.C < 1 || d.G < 1 || d.C % d.G != 0 || !(eps >= 0.f) || !std::isfinite(eps))
+        return DF2_ERR_INVALID_ARG;
+    if (d.G % 8 != 0 || d.C < 8 || d.C > 8192 || static_cast<long long>(d.B) * d.T > (1LL << 24))
+        return DF2_ERR_UNSUPPORTED;
+    if (!x || !base || !dyn || !y || !aligned(x, 16) || !aligned(base, 16) || !aligned(y, 16) || !aligned(dyn, 4) ||
+        (x_prev && !aligned(x_prev, 16)) || (gamma && !aligned(gamma, 16)))
+        return DF2_ERR_INVALID_ARG;
+    cudaGetLastError();
+    DF2_CUDA(launch_dynamic_conv(d.B, d.T, d.C, d.G, static_cast<const uint16_t *>(x),
+                                 static_cast<const uint16_t *>(x_prev), static_cast<const uint16_t *>(base), dyn,
+                                 static_cast<const uint16_t *>(gamma), eps, static_cast<uint16_t *>(y),
+                                 static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
 df2_status dflash2_check_device_status(void *workspace, size_t workspace_bytes, void *stream)
 {
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < kAlign)

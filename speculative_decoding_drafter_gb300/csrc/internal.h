@@ -57,6 +57,11 @@ cudaError_t launch_walk_sample(int B, int T, int k, const float *lattice, float 
                                const float *uniforms, int32_t *draft_ids, int32_t *n_draft, float *confidence,
                                cudaStream_t stream);
 
+// Two-tap dynamic depthwise conv of B blocks of T rows (bf16 [B*T, C] in and out).
+cudaError_t launch_dynamic_conv(int B, int T, int C, int G, const uint16_t *x, const uint16_t *x_prev,
+                                const uint16_t *base, const float *dyn, const uint16_t *gamma, float eps, uint16_t *y,
+                                cudaStream_t stream);
+
 // Greedy walk, one warp per sequence: draft_ids [B, T].
 cudaError_t launch_walk(int B, int T, int k, const float *lattice, int32_t *draft_ids, cudaStream_t stream);
 

@@ -21,15 +21,15 @@ __all__ = [
     "DFlash2Error", "Dims", "library", "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select",
     "dflash2_select_from_logits", "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice",
     "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
-    "dflash2_profile_events", "dflash2_topk_noalloc", "dflash2_walk_sample",
-    "EXPORTED_SYMBOLS",
+    "dflash2_profile_events", "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv",
+    "ConvDims", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select", "dflash2_select_from_logits",
     "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
     "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
-    "dflash2_topk_noalloc", "dflash2_walk_sample",
+    "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv",
 )
 
 
@@ -37,6 +37,10 @@ class DFlash2Error(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: status {status} ({_status_string(status)})")
+
+
+class ConvDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("C", ctypes.c_int32), ("G", ctypes.c_int32)]
 
 
 class Dims(ctypes.Structure):
@@ -79,6 +83,7 @@ def library(path: str | None = None):
                 "dflash2_profile_events": (I, [P, P]),
                 "dflash2_topk_noalloc": (I, [D, P, P, P, P]),
                 "dflash2_walk_sample": (I, [D, P, ctypes.c_float, ctypes.c_float, P, P, P, P, P]),
+                "dflash2_dynamic_conv": (I, [ctypes.POINTER(ConvDims), P, P, P, P, P, ctypes.c_float, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -327,6 +332,24 @@ def dflash2_walk_sample(lattice, B: int, T: int, k: int, *, temperature: float =
                                        _ptr(confidence, torch.float32, (B, T), "confidence"), _stream(stream))
     _check(st, "dflash2_walk_sample")
     return draft, n_draft, confidence
+
+
+def dflash2_dynamic_conv(x, base, dyn, T: int, *, x_prev=None, gamma=None, eps: float = 1e-6, G: int = 16, out=None,
+                         stream=None):
+    """Two-tap dynamic depthwise conv of B blocks of T rows: bf16 [B*T, C] -> bf16 [B*T, C]."""
+    R, C = x.shape
+    if R % T:
+        raise ValueError(f"x has {R} rows, not a multiple of T={T}")
+    B = R // T
+    d = ConvDims(B, T, C, G)
+    out = out if out is not None else torch.empty_like(x)
+    bf = torch.bfloat16
+    st = library().dflash2_dynamic_conv(ctypes.byref(d), _ptr(x, bf, (R, C), "x"), _ptr(x_prev, bf, (B, C), "x_prev"),
+                                        _ptr(base, bf, (2, C), "base"),
+                                        _ptr(dyn, torch.float32, (R, 2, C // G), "dyn"), _ptr(gamma, bf, (C,), "gamma"),
+                                        float(eps), _ptr(out, bf, (R, C), "y"), _stream(stream))
+    _check(st, "dflash2_dynamic_conv")
+    return out
 
 
 def dflash2_check_device_status(workspace: Workspace, stream=None) -> None:

@@ -42,7 +42,7 @@ from dataclasses import dataclass
 
 import numpy as np
 
-__all__ = ["SelectorConfig", "CONFIGS", "make_inputs", "bf16_bits_to_f32", "f32_to_bf16_bits"]
+__all__ = ["SelectorConfig", "CONFIGS", "make_inputs", "make_conv_inputs", "bf16_bits_to_f32", "f32_to_bf16_bits"]
 
 
 @dataclass(frozen=True)
@@ -198,3 +198,22 @@ def make_inputs(cfg: SelectorConfig | str, seed: int = 0) -> dict:
         "anchor": anchor,
         "plant": plant,
     }
+
+
+_T_CONV_X, _T_CONV_PREV, _T_CONV_BASE, _T_CONV_DYN, _T_CONV_GAMMA = range(21, 26)
+
+
+def make_conv_inputs(B: int, T: int, C: int, G: int = 16, seed: int = 0) -> dict:
+    """Seeded inputs of the dynamic local convolution of B blocks of T positions.
+
+    x [B*T, C] and x_prev [B, C] ~ N(0, 1); base [2, C] ~ N(0, 0.5); gamma [C] ~ 1 + N(0, 0.1)
+    (all bf16 bits); dyn [B*T, 2, C/G] ~ N(0, 0.1) float32 (already-projected corrections).
+    """
+    x = _normal_bf16(B * T, C, 1.0, seed, _T_CONV_X)
+    x_prev = _normal_bf16(B, C, 1.0, seed, _T_CONV_PREV)
+    base = _normal_bf16(2, C, 0.5, seed, _T_CONV_BASE)
+    gg = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _T_CONV_GAMMA])))
+    gamma = f32_to_bf16_bits((1.0 + 0.1 * gg.standard_normal(C)).astype(np.float32))
+    gd = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _T_CONV_DYN])))
+    dyn = (0.1 * gd.standard_normal((B * T, 2, C // G), dtype=np.float32)).astype(np.float32)
+    return {"x": x, "x_prev": x_prev, "base": base, "gamma": gamma, "dyn": dyn, "B": B, "T": T, "C": C, "G": G}

@@ -105,6 +105,16 @@ def test_stage_entry_points_reject_bad_arguments(lib):
                                    None) == DF2_ERR_INVALID_ARG
     assert lib.dflash2_walk_sample(ctypes.byref(d), None, 1.0, 0.5, None, 0x2000, None, None,
                                    None) == DF2_ERR_INVALID_ARG
+    from speculative_decoding_drafter_gb300.dflash2 import ConvDims
+
+    good = (0x1000, None, 0x2000, 0x3000, None, 1e-6, 0x4000, None)
+    assert lib.dflash2_dynamic_conv(ctypes.byref(ConvDims(2, 4, 40, 16)), *good) == DF2_ERR_INVALID_ARG  # C % G
+    assert lib.dflash2_dynamic_conv(ctypes.byref(ConvDims(2, 4, 48, 12)), *good) == DF2_ERR_UNSUPPORTED  # G % 8
+    assert lib.dflash2_dynamic_conv(ctypes.byref(ConvDims(2, 4, 16384, 16)), *good) == DF2_ERR_UNSUPPORTED
+    assert lib.dflash2_dynamic_conv(ctypes.byref(ConvDims(2, 4, 64, 16)), 0x1008, None, 0x2000, 0x3000, None, 1e-6,
+                                    0x4000, None) == DF2_ERR_INVALID_ARG  # x not 16-byte aligned
+    assert lib.dflash2_dynamic_conv(ctypes.byref(ConvDims(2, 4, 64, 16)), 0x1000, None, 0x2000, 0x3000, None, -1.0,
+                                    0x4000, None) == DF2_ERR_INVALID_ARG  # eps < 0
     assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100010, 1 << 40, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100000, 4096, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_workspace_init(ctypes.byref(dims(k=0)), 0x100000, 1 << 40, None) == DF2_ERR_INVALID_ARG

@@ -332,3 +332,43 @@ def test_walk_sample_greedy_reproduces_the_select_draft(case):
     assert np.all(host(n) == cfg.T)
     conf = host(c)
     assert np.all((conf > 0) & (conf <= 1.0 + 1e-6))
+
+
+# ---------------------------------------------------------------- dynamic local convolution
+
+from speculative_decoding_drafter_gb300.synth import make_conv_inputs  # noqa: E402
+
+
+def _conv_tol(ref):
+    """One bf16 ulp of the value (the output is rounded to bf16) plus float32 slack relative to the row."""
+    row = np.abs(ref).max(axis=1, keepdims=True)
+    return 2.0 ** -8 * np.abs(ref) + 2.0 ** -16 * row + 1e-30
+
+
+@pytest.mark.parametrize("B,T,C,G,prev,norm", [(2, 5, 64, 16, True, False), (3, 16, 4096, 16, True, True),
+                                               (1, 1, 8192, 16, False, True), (5, 7, 208, 16, True, True),
+                                               (4, 3, 96, 8, False, False), (1024, 16, 4096, 16, True, True)])
+def test_dynamic_conv_matches_oracle(B, T, C, G, prev, norm):
+    c = make_conv_inputs(B, T, C, G, seed=B + T + C)
+    xp = c["x_prev"] if prev else None
+    gm = c["gamma"] if norm else None
+    y = df.dflash2_dynamic_conv(dev_bf16(c["x"]), dev_bf16(c["base"]), dev(c["dyn"]), T,
+                                x_prev=None if xp is None else dev_bf16(xp), gamma=None if gm is None else dev_bf16(gm),
+                                eps=1e-6, G=G)
+    got = bf16_bits_to_f32(host(y.view(torch.int16)).view(np.uint16)).astype(np.float64)
+    ref = oracle.dynamic_conv(c["x"], xp, c["base"], c["dyn"], T, G, gamma=gm, eps=1e-6)
+    err = np.abs(got - ref)
+    assert np.all(err <= _conv_tol(ref)), f"max excess {(err - _conv_tol(ref)).max()}"
+
+
+def test_dynamic_conv_first_position_reads_only_its_own_block():
+    B, T, C, G = 3, 4, 128, 16
+    c = make_conv_inputs(B, T, C, G, seed=7)
+    x = c["x"].copy()
+    ident_prev = f32_to_bf16_bits(np.stack([np.zeros(C), np.ones(C)]).astype(np.float32))
+    zero = np.zeros_like(c["dyn"])
+    y = df.dflash2_dynamic_conv(dev_bf16(x), dev_bf16(ident_prev), dev(zero), T, x_prev=dev_bf16(c["x_prev"]), G=G)
+    got = host(y.view(torch.int16)).view(np.uint16)
+    for b in range(B):
+        assert np.array_equal(got[b * T], c["x_prev"][b])
+        assert np.array_equal(got[b * T + 1:(b + 1) * T], x[b * T:(b + 1) * T - 1])

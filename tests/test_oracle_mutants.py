@@ -41,6 +41,12 @@ MUTANTS = {
     "stop_counts_the_low_step": ("                n_draft[b] = (int32_t)t;", "                n_draft[b] = (int32_t)t + 1;"),
     "inverse_cdf_off_by_one": ("                    if (run > u) {\n                        pick = j;",
                                "                    if (run > u) {\n                        pick = j + 1 < k ? j + 1 : j;"),
+    "conv_taps_swapped": ("const double k0 = bf16_to_double(base[c])", "const double k0 = bf16_to_double(base[C + c])"),
+    "conv_group_interleaved": ("const int64_t g = c / G;", "const int64_t g = c % groups;"),
+    "conv_first_position_reads_zero": ("prv[c] = x_prev ? bf16_to_double(x_prev[b * C + c]) : 0.0;", "prv[c] = 0.0;"),
+    "conv_crosses_blocks": ("                if (t > 0)\n                    prv[c] = bf16_to_double(x[(r - 1) * C + c]);",
+                            "                if (r > 0)\n                    prv[c] = bf16_to_double(x[(r - 1) * C + c]);"),
+    "conv_norm_without_mean": ("1.0 / sqrt(sc / (double)C + eps)", "1.0 / sqrt(sc + eps)"),
     "gate_of_wrong_row": ("bf16_to_double(hidden[r * H + h]);\n            gate[r * D + d] = acc;",
                           "bf16_to_double(hidden[(R - 1 - r) * H + h]);\n            gate[r * D + d] = acc;"),
 }

@@ -436,3 +436,75 @@ def test_sampling_at_vanishing_temperature_is_greedy_and_shift_invariant():
     a = oracle.walk_sample(lat, B, T, k, temperature=0.9, uniforms=u)
     b = oracle.walk_sample(shifted, B, T, k, temperature=0.9, uniforms=u)
     assert np.array_equal(a[0], b[0]) and np.allclose(a[2], b[2], rtol=1e-12)
+
+
+# ---------------------------------------------------------------- dynamic local convolution
+
+
+def _conv_inputs(rng, B, T, C, G, with_prev=True):
+    x = rand_bf16(rng, (B * T, C))
+    xp = rand_bf16(rng, (B, C)) if with_prev else None
+    base = rand_bf16(rng, (2, C), 0.5)
+    dyn = (rng.standard_normal((B * T, 2, C // G)) * 0.1).astype(np.float32)
+    return x, xp, base, dyn
+
+
+def test_conv_identity_and_shift_taps():
+    rng = np.random.default_rng(41)
+    B, T, C, G = 3, 5, 32, 16
+    x, xp, _, _ = _conv_inputs(rng, B, T, C, G)
+    zero = np.zeros((B * T, 2, C // G), np.float32)
+    xf, xpf = bf16_bits_to_f32(x).astype(np.float64), bf16_bits_to_f32(xp).astype(np.float64)
+    ident = bf(np.stack([np.ones(C), np.zeros(C)]))
+    assert np.array_equal(oracle.dynamic_conv(x, xp, ident, zero, T, G), xf)
+    shift = bf(np.stack([np.zeros(C), np.ones(C)]))
+    y = oracle.dynamic_conv(x, xp, shift, zero, T, G)
+    for b in range(B):
+        assert np.array_equal(y[b * T], xpf[b])  # position 0 reads the last verified token
+        assert np.array_equal(y[b * T + 1:(b + 1) * T], xf[b * T:(b + 1) * T - 1])  # never the previous block
+    y0 = oracle.dynamic_conv(x, None, shift, zero, T, G)
+    assert np.all(y0[::T] == 0.0)
+
+
+def test_conv_dynamic_correction_is_shared_by_each_group_of_channels():
+    B, T, C, G = 2, 3, 48, 16
+    x = bf(np.ones((B * T, C)))
+    xp = bf(np.ones((B, C)))
+    base = bf(np.zeros((2, C)))
+    dyn = np.arange(B * T * 2 * (C // G), dtype=np.float32).reshape(B * T, 2, C // G)
+    y = oracle.dynamic_conv(x, xp, base, dyn, T, G)
+    for r in range(B * T):
+        for c in range(C):
+            assert y[r, c] == dyn[r, 0, c // G] + dyn[r, 1, c // G]
+
+
+def test_conv_tap_weights_combine_base_and_correction():
+    B, T, C, G = 1, 2, 16, 16
+    x = bf(np.full((B * T, C), 2.0))
+    xp = bf(np.full((B, C), 3.0))
+    base = bf(np.stack([np.full(C, 0.5), np.full(C, 0.25)]))
+    dyn = np.zeros((B * T, 2, 1), np.float32)
+    dyn[:, 0, 0], dyn[:, 1, 0] = 0.5, -0.25
+    y = oracle.dynamic_conv(x, xp, base, dyn, T, G)
+    # t=0: (0.5+0.5)*2 + (0.25-0.25)*3 = 2 ; t=1: 1*2 + 0*2 = 2
+    assert np.all(y == 2.0)
+    dyn[:, 1, 0] = 0.75
+    y = oracle.dynamic_conv(x, xp, base, dyn, T, G)
+    assert np.all(y[0] == 2.0 + 1.0 * 3.0) and np.all(y[1] == 2.0 + 1.0 * 2.0)
+
+
+def test_conv_rms_normalisation_is_scale_invariant_and_closed_form():
+    rng = np.random.default_rng(42)
+    B, T, C, G = 2, 4, 64, 16
+    x, xp, base, dyn = _conv_inputs(rng, B, T, C, G)
+    gamma = bf(np.ones(C))
+    y1 = oracle.dynamic_conv(x, xp, base, dyn, T, G, gamma=gamma, eps=0.0)
+    x4 = f32_to_bf16_bits(bf16_bits_to_f32(x) * np.float32(4.0))
+    xp4 = f32_to_bf16_bits(bf16_bits_to_f32(xp) * np.float32(4.0))
+    assert np.allclose(oracle.dynamic_conv(x4, xp4, base, dyn, T, G, gamma=gamma, eps=0.0), y1, rtol=1e-13, atol=0)
+    # a constant row a normalises to sign(a) * gamma
+    xc = bf(np.full((B * T, C), -3.0))
+    ident = bf(np.stack([np.ones(C), np.zeros(C)]))
+    g2 = bf(np.full(C, 2.0))
+    y = oracle.dynamic_conv(xc, None, ident, np.zeros_like(dyn), T, G, gamma=g2, eps=0.0)
+    assert np.allclose(y, -2.0, rtol=1e-15)
