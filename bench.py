@@ -47,8 +47,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="8b_b1", choices=list(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="select", choices=["select", "conv"],
-                    help="select: the selector head (default); conv: the dynamic local convolution")
+    ap.add_argument("--op", default="select", choices=["select", "conv", "topk"],
+                    help="select: the selector head (default); conv: the dynamic local convolution; "
+                         "topk: top-k A/B (fused epilogue vs materialised logits, ours vs torch.topk)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     a = ap.parse_args()
@@ -470,6 +471,88 @@ def run_conv(args, rank: int, world: int):
     return 0
 
 
+def run_topk(args, cfg, rank: int):
+    """Top-k A/B on one config: (a) dflash2_topk vs torch.topk over the same materialised float32
+    logits; (b) the fused LM head (top-k in the epilogue) vs materialising the logits and then
+    taking the top-k.  Prints one JSON line (rank 0)."""
+    import torch
+
+    from speculative_decoding_drafter_gb300 import dflash2 as df
+
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    peaks, peak_kind = load_peaks()
+    R, V, H, k = cfg.R, cfg.V, cfg.H, cfg.k
+    x = make_inputs(cfg, 0)
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    hidden, W = dev_bf16(x["hidden"]), dev_bf16(x["W_vocab"])
+    logits = torch.empty((R, V), dtype=torch.float32, device="cuda")
+    ws = df.Workspace(df.make_dims(R, 1, H, V, k, 8))
+    ids = torch.empty((R, k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, k), dtype=torch.float32, device="cuda")
+    df.dflash2_lm_head_logits(hidden, W, out=logits, workspace=ws)
+
+    def timed(fn, steps):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(steps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps * 1e3  # us
+
+    ours_us = timed(lambda: df.dflash2_topk(logits, k, ids=ids, vals=vals, workspace=ws), args.steps)
+    torch_us = timed(lambda: torch.topk(logits, k, dim=1, largest=True, sorted=True), args.steps)
+    tv, ti = torch.topk(logits, k, dim=1, largest=True, sorted=True)
+    df.dflash2_topk(logits, k, ids=ids, vals=vals, workspace=ws)
+    torch.cuda.synchronize()
+    same_vals = bool(torch.equal(tv, vals))
+    same_sets = bool(torch.equal(torch.sort(ti.to(torch.int32), dim=1)[0], torch.sort(ids, dim=1)[0]))
+    materialised_us = timed(lambda: (df.dflash2_lm_head_logits(hidden, W, out=logits, workspace=ws),
+                                     df.dflash2_topk(logits, k, ids=ids, vals=vals, workspace=ws)), args.steps)
+    # the fused path: the LM-head launch of dflash2_select (top-k in the epilogue; no logits in memory)
+    d = {n: dev_bf16(x[n]) for n in ("W_sel", "pred_cb", "succ_cb")}
+    anchor = torch.from_numpy(x["anchor"]).cuda()
+    wsel = df.Workspace(df.make_dims(cfg.B, cfg.T, H, V, k, cfg.D))
+    lat = torch.empty((R, k + k * k), dtype=torch.float32, device="cuda")
+    dr = torch.empty((cfg.B, cfg.T), dtype=torch.int32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.steps)]
+    for e in ev:
+        e.record()
+    for _ in range(args.warmup):
+        df.dflash2_select(hidden, W, d["W_sel"], d["pred_cb"], d["succ_cb"], anchor, k, cfg.T, lattice=lat,
+                          draft_ids=dr, workspace=wsel)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        df.dflash2_profile_events(ev[2 * i], ev[2 * i + 1])
+        df.dflash2_select(hidden, W, d["W_sel"], d["pred_cb"], d["succ_cb"], anchor, k, cfg.T, lattice=lat,
+                          draft_ids=dr, workspace=wsel)
+    torch.cuda.synchronize()
+    df.dflash2_profile_events(None, None)
+    fused_us = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.steps)) / args.steps * 1e3
+    read_gbs = R * V * 4 / (ours_us * 1e-6) / 1e9
+    print(json.dumps({
+        "impl": "ours", "op": "topk", "metric": "top-k of materialised float32 logits, us per call",
+        "value": ours_us, "unit": "us", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "logits_bytes": R * V * 4},
+        "torch_topk_us": torch_us, "speedup_vs_torch_topk": torch_us / ours_us,
+        "same_values_as_torch_topk": same_vals, "same_candidate_sets_as_torch_topk": same_sets,
+        "roofline": {"bound": "hbm", "achieved": read_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": read_gbs / peaks["hbm_gbs"], "kernel": "logits_topk_partial + topk_merge",
+                     "peak_source": peak_kind},
+        "lm_head_then_topk_us": materialised_us, "fused_lm_head_topk_gate_us": fused_us,
+        "fused_saving": 1.0 - fused_us / materialised_us}), flush=True)
+    return 0
+
+
 def main():
     args = parse_args()
     cfg = CONFIGS[args.config]
@@ -477,6 +560,8 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
     if args.op == "conv":
         return run_conv(args, rank, world)
+    if args.op == "topk":
+        return run_topk(args, cfg, rank)
     if args.impl == "reference":
         return run_reference(args, cfg, rank)
     return run_ours(args, cfg, rank, world)

@@ -15,9 +15,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-// One CTA per (row, column slice).  Each thread keeps a register top-KP over the
-// columns it reads (in increasing id order), each warp merges its 32 lists, and
-// warp 0 merges the 8 warp lists into the slice's partial list.
+// One CTA per (row, column slice), 8 warps.  Each warp keeps one warp-wide sorted list
+// (lane j holds entry j) over a contiguous part of the slice: lanes load 16-byte groups
+// (8 in flight per lane) and test them against the list's k-th entry, so only the rare
+// candidates that beat it are inserted (a per-thread list would diverge: some lane of the
+// warp would insert on almost every step).  A bitonic butterfly then merges the 8 warp
+// lists into the slice's partial list.
 template <int KP, bool kVec4>
 __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const float *__restrict__ logits, int V,
                                                                        int n_split, float *__restrict__ pval,
@@ -28,52 +31,66 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const float *row = logits + static_cast<long long>(r) * V;
-    ThreadTopK<KP> top;
-    top.init();
+    WarpList wl;
+    wl.init();
     if constexpr (kVec4) {
         const int groups = V / 4;
         const int g0 = static_cast<int>(static_cast<long long>(s) * groups / n_split);
         const int g1 = static_cast<int>(static_cast<long long>(s + 1) * groups / n_split);
+        const int w0 = g0 + static_cast<int>(static_cast<long long>(warp) * (g1 - g0) / kWarps);
+        const int w1 = g0 + static_cast<int>(static_cast<long long>(warp + 1) * (g1 - g0) / kWarps);
         const float4 *row4 = reinterpret_cast<const float4 *>(row);
-        for (int g = g0 + threadIdx.x; g < g1; g += kThreads) {
-            const float4 x = __ldcs(row4 + g);
-            const float thr = top.threshold();
-            if (x.x > thr || x.y > thr || x.z > thr || x.w > thr) {
-                top.push_increasing_id(x.x, 4 * g);
-                top.push_increasing_id(x.y, 4 * g + 1);
-                top.push_increasing_id(x.z, 4 * g + 2);
-                top.push_increasing_id(x.w, 4 * g + 3);
+        constexpr int kU = 8;  // 16-byte loads in flight per lane
+        for (int g = w0 + lane; g < w1 + lane; g += 32 * kU) {
+            float4 x[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int gi = g + 32 * u;
+                x[u] = gi < w1 ? __ldcs(row4 + gi) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int gi = g + 32 * u;
+                wl.offer(x[u].x, 4 * gi, KP);
+                wl.offer(x[u].y, 4 * gi + 1, KP);
+                wl.offer(x[u].z, 4 * gi + 2, KP);
+                wl.offer(x[u].w, 4 * gi + 3, KP);
             }
         }
     } else {
         const int e0 = static_cast<int>(static_cast<long long>(s) * V / n_split);
         const int e1 = static_cast<int>(static_cast<long long>(s + 1) * V / n_split);
-        for (int e = e0 + threadIdx.x; e < e1; e += kThreads)
-            top.push_increasing_id(__ldcs(row + e), e);
+        const int w0 = e0 + static_cast<int>(static_cast<long long>(warp) * (e1 - e0) / kWarps);
+        const int w1 = e0 + static_cast<int>(static_cast<long long>(warp + 1) * (e1 - e0) / kWarps);
+        for (int e = w0 + lane; e < w1 + lane; e += 32) {
+            const float x = e < w1 ? __ldcs(row + e) : -INFINITY;
+            wl.offer(x, e, KP);
+        }
     }
 
-    WarpList wl;
-    wl.init();
-#pragma unroll
-    for (int j = 0; j < KP; ++j)
-        wl.offer(top.v[j], top.i[j], KP);
-
+    // merge the 8 warp lists: lane l of warp 0 takes warp l's list, bitonic butterfly
     __shared__ float sv[kWarps][32];
     __shared__ int si[kWarps][32];
     sv[warp][lane] = wl.v;
     si[warp][lane] = wl.i;
     __syncthreads();
     if (warp == 0) {
-        WarpList fl;
-        fl.init();
-        for (int w = 0; w < kWarps; ++w) {
-            const bool in = lane < KP;
-            fl.offer(in ? sv[w][lane] : -INFINITY, in ? si[w][lane] : INT_MAX, KP);
+        float av[KP];
+        int ai[KP];
+        const int w = lane & (kWarps - 1);
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            av[j] = sv[w][j];
+            ai[j] = si[w][j];
         }
-        if (lane < KP) {
+        warp_merge_top<KP>(av, ai, kWarps - 1);
+        if (lane == 0) {
             const long long base = (static_cast<long long>(r) * n_split + s) * KP;
-            pval[base + lane] = fl.v;
-            pid[base + lane] = fl.i;
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                pval[base + j] = av[j];
+                pid[base + j] = ai[j];
+            }
         }
     }
 }
