@@ -10,10 +10,12 @@
 // Either segment may be empty (the stage entry points use the store segment alone).
 //
 // Design (one CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: an A box of the live rows (<= 128) and up to 256 rows of B,
-//               64 K-elements (128 bytes, 128-byte swizzle) per stage, 4-6 stages.
-//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N<=256,
-//               K=16 per instruction) into one of two 256-column accumulators.
+//   warp 0      TMA producer: per stage, kbs consecutive K-blocks of 64 elements (128
+//               bytes, 128-byte swizzle) of an A box of the live rows (<= 128) and of a
+//               chunk of bn (128 or 256) rows of B.  Up to 64 rows: bn = 128, kbs = 2
+//               (each W row read in 256-byte runs); beyond: bn = 256, kbs = 1.  4-6 stages.
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N<=bn,
+//               K=16 per instruction) into one of two bn-column accumulators.
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (thread = one row of C), then keep
 //               a per-row top-KP list in registers (full logits never reach global
 //               memory) or store float32.
@@ -36,11 +38,10 @@ namespace {
 
 constexpr int BM = 128;                        // rows of C per tile = TMEM lanes
 constexpr int BN = 256;                        // columns of C per chunk (MMA N, max)
-constexpr int BK = 64;                         // K elements per stage: one 128-byte swizzle row
+constexpr int BK = 64;                         // K elements per K-block: one 128-byte swizzle row
 constexpr int UNIT = 16;                       // column granularity of slices and of MMA N
 constexpr int MAX_STAGES = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;      // what one MMA reads of A: 16 KB
-constexpr int B_BYTES = BN * BK * 2;           // 32 KB
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int STASH_STRIDE = 33;               // floats per epilogue thread (32 + 1 pad)
@@ -56,6 +57,8 @@ struct GemmArgs {
     int n_store;      // columns of the store segment
     int row_tiles, n_split;
     int stages;       // pipeline depth
+    int bn;           // columns per chunk (128 or 256)
+    int kbs;          // K-blocks per stage
     int a_bytes;      // bytes of one A box (live rows x 128), a multiple of 1024
     float *pval;      // top-k lists [R, n_split, KP]
     int32_t *pid;
@@ -90,8 +93,8 @@ __device__ __forceinline__ Slice slice_of(const GemmArgs &g, int split)
     s.a1 = min(c_end, g.n_topk_pad);
     s.b0 = max(c_begin, g.n_topk_pad);
     s.b1 = c_end;
-    s.n0 = s.a1 > s.a0 ? (s.a1 - s.a0 + BN - 1) / BN : 0;
-    s.n1 = s.b1 > s.b0 ? (s.b1 - s.b0 + BN - 1) / BN : 0;
+    s.n0 = s.a1 > s.a0 ? (s.a1 - s.a0 + g.bn - 1) / g.bn : 0;
+    s.n1 = s.b1 > s.b0 ? (s.b1 - s.b0 + g.bn - 1) / g.bn : 0;
     return s;
 }
 
@@ -99,14 +102,14 @@ __device__ __forceinline__ Chunk chunk_of(const GemmArgs &g, const Slice &s, int
 {
     Chunk ch;
     if (c < s.n0) {
-        ch.c0 = s.a0 + c * BN;
-        ch.n = min(BN, s.a1 - ch.c0);
+        ch.c0 = s.a0 + c * g.bn;
+        ch.n = min(g.bn, s.a1 - ch.c0);
         ch.store = false;
         ch.b_row = ch.c0;
         ch.valid = max(0, min(ch.n, g.n_topk - ch.c0));
     } else {
-        ch.c0 = s.b0 + (c - s.n0) * BN;
-        ch.n = min(BN, s.b1 - ch.c0);
+        ch.c0 = s.b0 + (c - s.n0) * g.bn;
+        ch.n = min(g.bn, s.b1 - ch.c0);
         ch.store = true;
         ch.b_row = ch.c0 - g.n_topk_pad;
         ch.valid = max(0, min(ch.n, g.n_store - ch.b_row));
@@ -132,7 +135,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = args.stages;
-    const int stage_bytes = args.a_bytes + B_BYTES;
+    const int kbs = args.kbs;
+    const int b_sub = args.bn * BK * 2;  // bytes of one B K-block of a full chunk
+    // stage layout: kbs A K-blocks, then kbs B K-blocks (every part 1024-byte aligned)
+    const int stage_bytes = kbs * (args.a_bytes + b_sub);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
     // bars: full[MAX_STAGES] | empty[MAX_STAGES] | tfull[2] | tempty[2] | drain
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * MAX_STAGES + 5);
@@ -145,7 +151,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int split = blockIdx.x / args.row_tiles;
     const Slice slice = slice_of(args, split);
     const int n_chunks = slice.n0 + slice.n1;
-    const int kblocks = (args.K + BK - 1) / BK;
+    const int kstages = (args.K + BK * kbs - 1) / (BK * kbs);  // stages per chunk
 
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -197,22 +203,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const Chunk ch = chunk_of(args, slice, c);
                 const CUtensorMap *wide = ch.store ? &map_s_wide : &map_t_wide;
                 const CUtensorMap *narrow = ch.store ? &map_s_narrow : &map_t_narrow;
-                const uint32_t tx = static_cast<uint32_t>(args.a_bytes + ch.n * BK * 2);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                const uint32_t tx = static_cast<uint32_t>(kbs * (args.a_bytes + ch.n * BK * 2));
+                for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + stage * stage_bytes;
                     mbar_arrive_expect_tx(full_bar(stage), tx);
-                    tma_load_2d(smem_u32(st), &map_a, full_bar(stage), kb * BK, m_tile * BM);
-                    const uint32_t b_dst = smem_u32(st + args.a_bytes);
-                    if (ch.n == BN) {
-                        tma_load_2d(b_dst, wide, full_bar(stage), kb * BK, ch.b_row);
-                    } else {
-                        for (int q = 0; q < ch.n / UNIT; ++q)
-                            tma_load_2d(b_dst + q * UNIT * BK * 2, narrow, full_bar(stage), kb * BK,
-                                        ch.b_row + q * UNIT);
+                    for (int q = 0; q < kbs; ++q) {
+                        const int x = (ks * kbs + q) * BK;  // past K the boxes read zeros
+                        tma_load_2d(smem_u32(st + q * args.a_bytes), &map_a, full_bar(stage), x, m_tile * BM);
+                        const uint32_t b_dst = smem_u32(st + kbs * args.a_bytes + q * b_sub);
+                        if (ch.n == args.bn) {
+                            tma_load_2d(b_dst, wide, full_bar(stage), x, ch.b_row);
+                        } else {
+                            for (int u = 0; u < ch.n / UNIT; ++u)
+                                tma_load_2d(b_dst + u * UNIT * BK * 2, narrow, full_bar(stage), x, ch.b_row + u * UNIT);
+                        }
                     }
                     ++issued;
                     if (++stage == stages) {
@@ -244,19 +252,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int kb = 0; kb < kblocks; ++kb) {
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * args.bn);
+                for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(smem + stage * stage_bytes);
-                    const uint32_t b0 = a0 + static_cast<uint32_t>(args.a_bytes);
+                    const uint32_t st = smem_u32(smem + stage * stage_bytes);
+                    for (int q = 0; q < kbs; ++q) {
+                        const uint32_t a0 = st + static_cast<uint32_t>(q * args.a_bytes);
+                        const uint32_t b0 = st + static_cast<uint32_t>(kbs * args.a_bytes + q * b_sub);
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)
-                        umma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
-                                  (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
+                                      idesc, (ks | q | kk) != 0 ? 1u : 0u);
+                    }
                     umma_commit(empty_bar(stage));
                     if (++stage == stages) {
                         stage = 0;
@@ -291,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int cb = 0; cb < ch.n / 32 + ((ch.n & 31) ? 1 : 0); ++cb) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(buf * BN + cb * 32),
+                                       static_cast<uint32_t>(buf * args.bn + cb * 32),
                                    r);
                 tmem_wait_ld(r);
                 const int valid = min(32, ch.valid - cb * 32);
@@ -394,9 +405,15 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     // 128 rows, the rows past the box hold stale shared memory and only feed unused rows of C.
     const int a_rows = std::min(BM, (std::max(R, 1) + 7) / 8 * 8);
     args.a_bytes = a_rows * BK * 2;
-    const int stage_bytes = args.a_bytes + B_BYTES;
+    // Up to 64 rows the stream of W sets the time: 128-column chunks with 2 K-blocks per
+    // stage read each W row in 256-byte runs (measured on GB300: 193.5 vs 199.8 us for the
+    // 8B-class head at 16 rows).  Beyond, 256-column chunks with 1 K-block per stage feed
+    // the tensor cores best (438.5 vs 480.3 us at 512 rows).
+    args.bn = R <= 64 ? 128 : BN;
+    args.kbs = R <= 64 ? 2 : 1;
+    const int stage_bytes = args.kbs * (args.a_bytes + args.bn * BK * 2);
     args.stages = std::min(MAX_STAGES, STAGE_BUDGET / stage_bytes);
-    if (args.stages < 2 || stage_bytes < A_TILE_BYTES)
+    if (args.stages < 2 || args.a_bytes + args.bn * BK * 2 < A_TILE_BYTES)
         return cudaErrorInvalidConfiguration;
     const int smem_bytes = 1024 + args.stages * stage_bytes + BAR_BYTES + STASH_BYTES;
 
@@ -409,8 +426,9 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     const int tn = n_topk > 0 ? n_topk : n_store;
     const void *sb = n_store > 0 ? Bs : Bt;
     const int sn = n_store > 0 ? n_store : n_topk;
-    if ((e = make_map(&mtw, tb, K, tn, BN)) != cudaSuccess || (e = make_map(&mtn, tb, K, tn, UNIT)) != cudaSuccess ||
-        (e = make_map(&msw, sb, K, sn, BN)) != cudaSuccess || (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
+    if ((e = make_map(&mtw, tb, K, tn, args.bn)) != cudaSuccess ||
+        (e = make_map(&mtn, tb, K, tn, UNIT)) != cudaSuccess ||
+        (e = make_map(&msw, sb, K, sn, args.bn)) != cudaSuccess || (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
         return e;
     auto kern = gemm_tc_kernel<KP>;
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
