@@ -24,9 +24,10 @@
  * predecessor = anchor).
  *
  * Conventions shared by every entry point:
- *  - Every tensor pointer is a DEVICE pointer owned by the caller.  The
- *    library allocates nothing, frees nothing, and never synchronises a
- *    stream (except dflash2_check_device_status, which says so).
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller (except
+ *    the *_host arguments of dflash2_select_host).  The library allocates
+ *    nothing, frees nothing, and never synchronises a stream (except
+ *    dflash2_check_device_status and dflash2_select_host, which say so).
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *    the legacy default stream).  The returned status covers argument
  *    validation and launch errors (cudaGetLastError after enqueue); it does
@@ -130,6 +131,32 @@ DF2_API df2_status dflash2_select_from_logits(const df2_dims *dims, const float 
                                       const int32_t *anchor, float *lattice, int32_t *draft_ids,
                                       int32_t *topk_ids, float *topk_logits, float *gate, void *workspace,
                                       size_t workspace_bytes, void *stream);
+
+/*
+ * dflash2_select for a caller whose step inputs and results live in host memory (the
+ * drafting loop of a serving engine that feeds hidden states in and reads the draft out
+ * each step).  One call enqueues, on `stream`: the copy of hidden and anchor to device
+ * staging inside the workspace, the same two launches as dflash2_select, the copies of
+ * draft_ids (and of the lattice, if lattice_host is not NULL) back to host, and a copy of
+ * the device status word; it then waits for the stream.  Unlike every other call it
+ * returns only when the results are in host memory, and it also reports
+ * DF2_ERR_TIMEOUT from the device status word (then re-initialise the workspace).
+ *   hidden_host    bf16 [B*T, H], host memory
+ *   anchor_host    int32 [B], host memory
+ *   W_vocab, W_sel, pred_cb, succ_cb   device memory, as for dflash2_select
+ *   lattice_host   float [B*T, k + k*k] host memory, or NULL to skip its copy
+ *   draft_ids_host int32 [B*T] host memory
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) so that the
+ * copies run asynchronously; pageable memory works but serialises the host on each copy.
+ * The workspace must hold dflash2_select_host_workspace_bytes(dims): the
+ * dflash2_workspace_bytes layout followed by the device staging of hidden, anchor,
+ * lattice and draft.  Nothing is allocated.
+ */
+DF2_API size_t dflash2_select_host_workspace_bytes(const df2_dims *dims);
+DF2_API df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, const void *W_vocab,
+                                       const void *W_sel, const void *pred_cb, const void *succ_cb,
+                                       const int32_t *anchor_host, float *lattice_host, int32_t *draft_ids_host,
+                                       void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---- single steps of the path (same kernels as above), for stage-by-stage checks ---- */
 

@@ -1,6 +1,6 @@
 // api.cu -- the C ABI declared in include/dflash2.h: argument checks, workspace
 // carving and the launch sequence of the selector head.  No allocation, no sync
-// (except dflash2_check_device_status).
+// (except dflash2_check_device_status and dflash2_select_host).
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -87,6 +87,35 @@ Workspace carve(const df2_dims &d, void *base)
     off += round_up(R * d.D * sizeof(float));
     w.bytes = off;
     return w;
+}
+
+// Device staging of dflash2_select_host, placed after the select workspace (each part
+// 256-byte aligned): hidden [R, H] bf16 | anchor [B] | lattice [R, k + k*k] | draft [R].
+struct Staging {
+    uint16_t *hidden;
+    int32_t *anchor;
+    float *lattice;
+    int32_t *draft;
+    size_t bytes;  // select workspace + staging
+};
+
+Staging carve_staging(const df2_dims &d, void *base)
+{
+    const size_t R = static_cast<size_t>(d.B) * d.T;
+    const size_t width = static_cast<size_t>(d.k) + static_cast<size_t>(d.k) * d.k;
+    uint8_t *p = static_cast<uint8_t *>(base);
+    Staging s{};
+    size_t off = carve(d, nullptr).bytes;
+    s.hidden = reinterpret_cast<uint16_t *>(p ? p + off : nullptr);
+    off += round_up(R * d.H * sizeof(uint16_t));
+    s.anchor = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
+    off += round_up(static_cast<size_t>(d.B) * sizeof(int32_t));
+    s.lattice = reinterpret_cast<float *>(p ? p + off : nullptr);
+    off += round_up(R * width * sizeof(float));
+    s.draft = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
+    off += round_up(R * sizeof(int32_t));
+    s.bytes = off;
+    return s;
 }
 
 df2_status check_workspace(const df2_dims &d, void *ws, size_t bytes)
@@ -186,6 +215,44 @@ df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *
                             st));
     DF2_CUDA(profile_mark(t_profile_end, st));
     return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st);
+}
+
+size_t dflash2_select_host_workspace_bytes(const df2_dims *dims)
+{
+    if (check_dims(dims) != DF2_OK)
+        return 0;
+    return carve_staging(*dims, nullptr).bytes;
+}
+
+df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, const void *W_vocab, const void *W_sel,
+                               const void *pred_cb, const void *succ_cb, const int32_t *anchor_host,
+                               float *lattice_host, int32_t *draft_ids_host, void *workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    if (!hidden_host || !anchor_host || !draft_ids_host || !W_vocab || !aligned(W_vocab, 16))
+        return DF2_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < carve_staging(d, nullptr).bytes)
+        return DF2_ERR_WORKSPACE;
+    const Staging s = carve_staging(d, workspace);
+    const size_t R = static_cast<size_t>(d.B) * d.T;
+    const size_t width = static_cast<size_t>(d.k) + static_cast<size_t>(d.k) * d.k;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    DF2_CUDA(cudaMemcpyAsync(s.hidden, hidden_host, R * d.H * sizeof(uint16_t), cudaMemcpyHostToDevice, st));
+    DF2_CUDA(cudaMemcpyAsync(s.anchor, anchor_host, d.B * sizeof(int32_t), cudaMemcpyHostToDevice, st));
+    DF2_TRY(dflash2_select(dims, s.hidden, W_vocab, W_sel, pred_cb, succ_cb, s.anchor, s.lattice, s.draft, nullptr,
+                           nullptr, nullptr, workspace, workspace_bytes, stream));
+    DF2_CUDA(cudaMemcpyAsync(draft_ids_host, s.draft, R * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
+    if (lattice_host)
+        DF2_CUDA(cudaMemcpyAsync(lattice_host, s.lattice, R * width * sizeof(float), cudaMemcpyDeviceToHost, st));
+    // The status word comes back behind the results; a stack destination is pageable
+    // memory, for which the copy returns only once it is complete.
+    uint32_t word = 0;
+    DF2_CUDA(cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st));
+    DF2_CUDA(cudaStreamSynchronize(st));
+    return word == 0 ? DF2_OK : DF2_ERR_TIMEOUT;
 }
 
 df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits, const void *hidden,

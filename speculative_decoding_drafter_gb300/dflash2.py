@@ -22,14 +22,16 @@ __all__ = [
     "dflash2_select_from_logits", "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice",
     "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
     "dflash2_profile_events", "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv",
-    "ConvDims", "EXPORTED_SYMBOLS",
+    "ConvDims", "EXPORTED_SYMBOLS", "dflash2_select_host", "dflash2_select_host_workspace_bytes", "HostWorkspace",
+    "SelectHostPlan",
 ]
 
 EXPORTED_SYMBOLS = (
     "dflash2_workspace_bytes", "dflash2_workspace_init", "dflash2_select", "dflash2_select_from_logits",
     "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
     "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
-    "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv",
+    "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv", "dflash2_select_host",
+    "dflash2_select_host_workspace_bytes",
 )
 
 
@@ -84,6 +86,8 @@ def library(path: str | None = None):
                 "dflash2_topk_noalloc": (I, [D, P, P, P, P]),
                 "dflash2_walk_sample": (I, [D, P, ctypes.c_float, ctypes.c_float, P, P, P, P, P]),
                 "dflash2_dynamic_conv": (I, [ctypes.POINTER(ConvDims), P, P, P, P, P, ctypes.c_float, P, P]),
+                "dflash2_select_host": (I, [D, P, P, P, P, P, P, P, P, P, S, P]),
+                "dflash2_select_host_workspace_bytes": (S, [D]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -166,6 +170,39 @@ class Workspace:
         return self.view.data_ptr()
 
 
+class HostWorkspace(Workspace):
+    """Workspace of dflash2_select_host: the select workspace plus device staging of the
+    host-side inputs and results."""
+
+    def __init__(self, dims: Dims, device=None):
+        n = dflash2_select_host_workspace_bytes(dims)
+        if n == 0:
+            raise ValueError(f"invalid or unsupported dims {dims}")
+        self.dims = dims
+        self.tensor = torch.zeros(n + 256, dtype=torch.uint8, device=device or "cuda")
+        off = (-self.tensor.data_ptr()) % 256
+        self.view = self.tensor[off:off + n]
+        self.nbytes = n
+
+
+def dflash2_select_host_workspace_bytes(dims: Dims) -> int:
+    return int(library().dflash2_select_host_workspace_bytes(ctypes.byref(dims)))
+
+
+def _host_ptr(t, dtype, shape, name):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise TypeError(f"{name} must be a CPU tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
 def _workspace(ws, dims, device):
     if ws is None:
         return Workspace(dims, device)
@@ -202,6 +239,69 @@ def dflash2_select(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: 
         _ptr(gate, torch.float32, (R, d.D), "gate"), ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "dflash2_select")
     return lattice, draft_ids
+
+
+def _select_host_args(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k, T, lattice_host,
+                      draft_ids_host, workspace, stream):
+    """Checks the arguments of dflash2_select_host once; returns (args tuple, tensors kept alive)."""
+    d = _dims_of(hidden_host, W_vocab, W_sel, pred_cb, k, T)
+    R = d.B * d.T
+    if lattice_host is None:
+        lattice_host = torch.empty((R, k + k * k), dtype=torch.float32).pin_memory()
+    elif lattice_host is False:
+        lattice_host = None
+    if draft_ids_host is None:
+        draft_ids_host = torch.empty((d.B, T), dtype=torch.int32).pin_memory()
+    if workspace is None:
+        workspace = HostWorkspace(d, W_vocab.device)
+    elif workspace.nbytes < dflash2_select_host_workspace_bytes(d):
+        raise ValueError("workspace too small for dflash2_select_host with these dims")
+    bf = torch.bfloat16
+    args = (ctypes.byref(d), _host_ptr(hidden_host, bf, (R, d.H), "hidden_host"),
+            _ptr(W_vocab, bf, (d.V, d.H), "W_vocab"), _ptr(W_sel, bf, (d.D, d.H), "W_sel"),
+            _ptr(pred_cb, bf, (d.V, d.D), "pred_cb"), _ptr(succ_cb, bf, (d.V, d.D), "succ_cb"),
+            _host_ptr(anchor_host, torch.int32, (d.B,), "anchor_host"),
+            _host_ptr(lattice_host, torch.float32, (R, k + k * k), "lattice_host"),
+            _host_ptr(draft_ids_host, torch.int32, (d.B, T), "draft_ids_host"), workspace.ptr, workspace.nbytes,
+            _stream(stream))
+    keep = (d, hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, workspace)
+    return args, keep, lattice_host, draft_ids_host
+
+
+def dflash2_select_host(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k: int, T: int, *,
+                        lattice_host=None, draft_ids_host=None, workspace: HostWorkspace | None = None, stream=None):
+    """Selector head with host-memory inputs and results (pin them for asynchronous copies).
+
+    hidden_host bf16 [B*T, H] and anchor_host int32 [B] are CPU tensors; the weights are CUDA
+    tensors.  Returns (lattice_host or None, draft_ids_host [B, T] int32), filled when the call
+    returns.  Pass lattice_host=False to skip the lattice copy.
+    """
+    args, _keep, lattice_host, draft_ids_host = _select_host_args(
+        hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k, T, lattice_host, draft_ids_host, workspace,
+        stream)
+    _check(library().dflash2_select_host(*args), "dflash2_select_host")
+    return lattice_host, draft_ids_host
+
+
+class SelectHostPlan:
+    """dflash2_select_host with its buffers bound once, for a drafting loop that refills the
+    same host buffers every step: the arguments are checked here, and each call is a single
+    C call (the per-call checks of the function above cost as much as a kernel launch).
+    The bound tensors are kept alive; write the next step's hidden states and anchors into
+    them in place.  Calling returns (lattice_host or None, draft_ids_host)."""
+
+    def __init__(self, hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k: int, T: int, *,
+                 lattice_host=None, draft_ids_host=None, workspace: HostWorkspace | None = None, stream=None):
+        self._args, self._keep, self.lattice_host, self.draft_ids_host = _select_host_args(
+            hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k, T, lattice_host, draft_ids_host,
+            workspace, stream)
+        self._fn = library().dflash2_select_host
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st:
+            raise DFlash2Error(st, "dflash2_select_host")
+        return self.lattice_host, self.draft_ids_host
 
 
 def dflash2_select_from_logits(logits, hidden, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, lattice=None,

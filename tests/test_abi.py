@@ -118,3 +118,30 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100010, 1 << 40, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_workspace_init(ctypes.byref(d), 0x100000, 4096, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_workspace_init(ctypes.byref(dims(k=0)), 0x100000, 1 << 40, None) == DF2_ERR_INVALID_ARG
+
+
+def test_select_host_workspace_and_rejections(lib):
+    # Pointer values below are never dereferenced: every case fails validation first.
+    from speculative_decoding_drafter_gb300.dflash2 import (dflash2_select_host_workspace_bytes,
+                                                            dflash2_workspace_bytes)
+
+    d = dims()
+    R, H, B, k = d.B * d.T, d.H, d.B, d.k
+    base = dflash2_workspace_bytes(d)
+    n = dflash2_select_host_workspace_bytes(d)
+    assert n % 256 == 0
+    assert n >= base + R * H * 2 + B * 4 + R * (k + k * k) * 4 + R * 4
+    assert dflash2_select_host_workspace_bytes(dims(k=0)) == 0
+    h, w, a, lat, dr = 0x300000, 0x200000, 0x310000, 0x320000, 0x330000
+
+    def call(dd=d, hidden=h, anchor=a, draft=dr, ws=0x100000, ws_bytes=n, W_vocab=w):
+        return lib.dflash2_select_host(ctypes.byref(dd), hidden, W_vocab, w, w, w, anchor, lat, draft, ws, ws_bytes,
+                                       None)
+
+    assert call(hidden=None) == DF2_ERR_INVALID_ARG
+    assert call(anchor=None) == DF2_ERR_INVALID_ARG
+    assert call(draft=None) == DF2_ERR_INVALID_ARG
+    assert call(W_vocab=0x200008) == DF2_ERR_INVALID_ARG
+    assert call(dd=dims(k=0)) == DF2_ERR_INVALID_ARG
+    assert call(ws_bytes=base) == DF2_ERR_WORKSPACE  # room for dflash2_select only, not the staging
+    assert call(ws=0x100010) == DF2_ERR_WORKSPACE

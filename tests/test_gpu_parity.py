@@ -122,6 +122,34 @@ def test_select_is_deterministic(case):
     assert np.array_equal(host(draft), case["draft"])
 
 
+def test_select_host_matches_the_device_path(case):
+    """Host buffers in and out: the same kernels on staged copies, so the same bits."""
+    cfg, x, d = case["cfg"], case["x"], case["d"]
+    h_hidden = torch.from_numpy(x["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_anchor = torch.from_numpy(x["anchor"]).pin_memory()
+    hw = df.HostWorkspace(df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, cfg.k, cfg.D))
+    lat, draft = df.dflash2_select_host(h_hidden, d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], h_anchor,
+                                        cfg.k, cfg.T, workspace=hw)
+    assert np.array_equal(lat.numpy().view(np.uint32), case["lat"].view(np.uint32))
+    assert np.array_equal(draft.numpy(), case["draft"])
+    # again on the same workspace, without the lattice copy, into a pageable buffer
+    draft2 = torch.full((cfg.B, cfg.T), -7, dtype=torch.int32)
+    none, draft2 = df.dflash2_select_host(h_hidden, d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], h_anchor,
+                                          cfg.k, cfg.T, lattice_host=False, draft_ids_host=draft2, workspace=hw)
+    assert none is None
+    assert np.array_equal(draft2.numpy(), case["draft"])
+    # bound once, called twice; the second call sees hidden states rewritten in place
+    plan = df.SelectHostPlan(h_hidden, d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], h_anchor, cfg.k, cfg.T,
+                             workspace=hw)
+    lat3, draft3 = plan()
+    assert np.array_equal(lat3.numpy().view(np.uint32), case["lat"].view(np.uint32))
+    assert np.array_equal(draft3.numpy(), case["draft"])
+    h_hidden.zero_()
+    lat4, _ = plan()
+    k = cfg.k
+    assert np.array_equal(lat4.numpy()[:, :k], np.tile(np.arange(k, dtype=np.float32), (cfg.R, 1)))  # all-zero logits
+
+
 def test_duplicate_logits_break_ties_by_lower_id(case):
     if case["cfg"].plant != "dup_logits":
         pytest.skip("config has no duplicate logits")
