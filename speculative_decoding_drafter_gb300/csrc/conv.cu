@@ -9,13 +9,14 @@
 // The dynamic corrections arrive already projected (dyn [B*T, 2, C/G], float); the
 // optional RMS normalisation of the conv input (gamma) is fused in.
 //
-// A CTA takes up to 8 consecutive rows of one block, one warp per row.  It stages those
-// rows and the row before the first (the block's previous row, or the last verified
-// token, or zeros) in shared memory with one batch of cp.async copies, so each row is
-// read from DRAM once and a row's predecessor is the neighbouring warp's slot.  Each warp
-// reduces its own row's sum of squares (shuffles) and publishes it; after one CTA barrier
-// every warp has both RMS values and writes its bf16 output.  HBM-bound: per row 2C
-// bytes read, 2C written, C/G*8 bytes of corrections (read through L1).
+// A CTA takes up to 8 consecutive rows of one block.  It stages those rows and the row
+// before the first (the block's previous row, or the last verified token, or zeros) in
+// shared memory with one batch of cp.async copies, so each row is read from DRAM once.
+// Each thread then owns 16-byte channel chunks across all of the CTA's rows: the static
+// taps and gamma of a chunk are unpacked once and serve every row, and a row's normalised
+// input, kept in registers, is the next row's predecessor term.  The RMS of each staged
+// row comes from a CTA-wide reduction.  HBM-bound: per row 2C bytes read, 2C written,
+// C/G*8 bytes of corrections (read through L1).
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -74,12 +75,16 @@ __device__ __forceinline__ float inv_rms(float sumsq, int C, float eps)
     return (sumsq > 0.f || eps > 0.f) ? 1.f / sqrtf(sumsq / static_cast<float>(C) + eps) : 0.f;
 }
 
-__global__ void __launch_bounds__(kThreads) dynamic_conv_kernel(const ConvArgs a)
+constexpr int kSlots = kRowsPerCta + 1;
+
+__global__ void __launch_bounds__(kThreads, 3) dynamic_conv_kernel(const ConvArgs a)
 {
-    extern __shared__ __align__(16) uint4 rows[];  // slot 0: predecessor of the first row; slot 1+w: row t0+w
-    __shared__ float s_sumsq[kRowsPerCta + 1];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    extern __shared__ __align__(16) uint4 rows[];  // slot 0: predecessor of the first row; slot 1+s: row t0+s
+    __shared__ float s_part[kThreads / 32][16];    // per-warp partial sums of squares, by slot
+    __shared__ float s_scale[kSlots];              // 1/RMS of each slot (1 without normalisation)
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int b = blockIdx.x / a.tiles;
     const int t0 = (blockIdx.x - b * a.tiles) * kRowsPerCta;
     const int n = min(kRowsPerCta, a.T - t0);
@@ -87,95 +92,113 @@ __global__ void __launch_bounds__(kThreads) dynamic_conv_kernel(const ConvArgs a
     const int chunks = C / 8;
     const long long row0 = static_cast<long long>(b) * a.T + t0;  // global index of row t0
 
-    // ---- stage rows t0-1 .. t0+n-1: warp w copies its own row into slot w+1, warp 0 also
-    // the predecessor of row t0 into slot 0 (the block's previous row, the last verified
-    // token, or zeros).  A warp reads another warp's slot only after the CTA barrier below.
+    // ---- stage slots 0..n: rows t0-1 .. t0+n-1, consecutive in x except the predecessor
+    // of t0 = 0, which is the last verified token (x_prev) or zeros
     const uint4 *xs = reinterpret_cast<const uint4 *>(a.x);
-    auto stage = [&](int s) {
-        uint4 *dst = rows + static_cast<size_t>(s) * chunks;
-        const uint4 *src = nullptr;
-        if (s > 0)
-            src = xs + (row0 + s - 1) * chunks;
-        else if (t0 > 0)
-            src = xs + (row0 - 1) * chunks;
-        else if (a.x_prev)
-            src = reinterpret_cast<const uint4 *>(a.x_prev) + static_cast<long long>(b) * chunks;
-        for (int i = lane; i < chunks; i += 32) {
-            if (src)
-                cp_async16(dst + i, src + i);
-            else
-                dst[i] = make_uint4(0, 0, 0, 0);
-        }
-    };
-    if (warp < n)
-        stage(warp + 1);
-    if (warp == 0)
-        stage(0);
-    cp_async_commit_and_wait_all();
-    __syncwarp();
-
-    // ---- sums of squares of the warp's own slots (for the RMS normalisation)
-    auto slot_sumsq = [&](int s) {
-        float sq = 0.f;
-        const uint4 *v = rows + static_cast<size_t>(s) * chunks;
-        for (int i = lane; i < chunks; i += 32) {
-            float f[8];
-            unpack8(v[i], f);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                sq = fmaf(f[e], f[e], sq);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        if (lane == 0)
-            s_sumsq[s] = sq;
-    };
-    if (a.gamma) {
-        if (warp < n)
-            slot_sumsq(warp + 1);
-        if (warp == 0)
-            slot_sumsq(0);
+    const uint4 *src0 = t0 > 0 ? xs + (row0 - 1) * chunks
+                               : (a.x_prev ? reinterpret_cast<const uint4 *>(a.x_prev) + static_cast<long long>(b) * chunks
+                                           : nullptr);
+    for (int i = tid; i < chunks; i += kThreads) {
+        if (src0)
+            cp_async16(rows + i, src0 + i);
+        else
+            rows[i] = make_uint4(0, 0, 0, 0);
     }
+    const uint4 *src1 = xs + row0 * chunks;
+    for (int i = tid; i < n * chunks; i += kThreads)
+        cp_async16(rows + chunks + i, src1 + i);
+    cp_async_commit_and_wait_all();
     __syncthreads();
-    if (warp >= n)
-        return;
 
-    // ---- output of row t0 + warp
-    const long long r = row0 + warp;
-    const uint4 *cur = rows + static_cast<size_t>(warp + 1) * chunks;
-    const uint4 *prv = rows + static_cast<size_t>(warp) * chunks;
-    const float ic = a.gamma ? inv_rms(s_sumsq[warp + 1], C, a.eps) : 1.f;
-    const float ip = a.gamma ? inv_rms(s_sumsq[warp], C, a.eps) : 1.f;
+    // ---- 1/RMS of every slot (for the normalisation of the conv input)
+    if (a.gamma) {
+        float sq[kSlots];
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s)
+            sq[s] = 0.f;
+        for (int i = tid; i < chunks; i += kThreads) {
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s) {
+                if (s <= n) {
+                    float f[8];
+                    unpack8(rows[s * chunks + i], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        sq[s] = fmaf(f[e], f[e], sq[s]);
+                }
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < kSlots; ++s) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                sq[s] += __shfl_xor_sync(0xffffffffu, sq[s], off);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < kSlots; ++s)
+                s_part[warp][s] = sq[s];
+        }
+        __syncthreads();
+        if (tid <= n) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; ++w)
+                tot += s_part[w][tid];
+            s_scale[tid] = inv_rms(tot, C, a.eps);
+        }
+        __syncthreads();
+    }
+
+    // ---- outputs: y_t = (base0 + dyn0_t) * u_t + (base1 + dyn1_t) * u_{t-1}, u = gamma * x / RMS(x)
     const int groups = C / a.G;
     const int chunks_per_group = a.G / 8;  // G is a multiple of 8: a chunk never straddles groups
-    const float *d0 = a.dyn + r * 2 * groups;
-    const float *d1 = d0 + groups;
     const uint4 *b0p = reinterpret_cast<const uint4 *>(a.base);
     const uint4 *b1p = b0p + chunks;
     const uint4 *gp = reinterpret_cast<const uint4 *>(a.gamma);
-    uint4 *out = reinterpret_cast<uint4 *>(a.y) + r * chunks;
-    for (int i = lane; i < chunks; i += 32) {
+    uint4 *out = reinterpret_cast<uint4 *>(a.y) + row0 * chunks;
+    const float *dyn = a.dyn + row0 * 2 * groups;
+    for (int i = tid; i < chunks; i += kThreads) {
         const int g = i / chunks_per_group;
-        const float k0d = __ldg(d0 + g), k1d = __ldg(d1 + g);
-        float fc[8], fp[8], w0[8], w1[8];
-        unpack8(cur[i], fc);
-        unpack8(prv[i], fp);
+        // every row's corrections first: one memory latency per chunk, not one per row
+        float k0d[kRowsPerCta], k1d[kRowsPerCta];
+#pragma unroll
+        for (int s = 0; s < kRowsPerCta; ++s) {
+            k0d[s] = s < n ? __ldg(dyn + (2 * s) * groups + g) : 0.f;
+            k1d[s] = s < n ? __ldg(dyn + (2 * s + 1) * groups + g) : 0.f;
+        }
+        float w0[8], w1[8], gg[8], up[8];
         unpack8(__ldg(b0p + i), w0);
         unpack8(__ldg(b1p + i), w1);
-        float yv[8];
+        unpack8(rows[i], up);
         if (a.gamma) {
-            float gg[8];
             unpack8(__ldg(gp + i), gg);
+            const float sc = s_scale[0];
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                yv[e] = fmaf((w1[e] + k1d) * ip, fp[e] * gg[e], ((w0[e] + k0d) * ic) * (fc[e] * gg[e]));
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                yv[e] = fmaf(w1[e] + k1d, fp[e], (w0[e] + k0d) * fc[e]);
+                up[e] = up[e] * gg[e] * sc;
         }
-        __stcs(out + i, make_uint4(pack2(yv[0], yv[1]), pack2(yv[2], yv[3]), pack2(yv[4], yv[5]), pack2(yv[6], yv[7])));
+#pragma unroll
+        for (int s = 0; s < kRowsPerCta; ++s) {
+            if (s >= n)
+                break;
+            float u[8];
+            unpack8(rows[(s + 1) * chunks + i], u);
+            if (a.gamma) {
+                const float sc = s_scale[s + 1];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    u[e] = u[e] * gg[e] * sc;
+            }
+            float yv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                yv[e] = fmaf(w1[e] + k1d[s], up[e], (w0[e] + k0d[s]) * u[e]);
+                up[e] = u[e];
+            }
+            __stcs(out + s * chunks + i,
+                   make_uint4(pack2(yv[0], yv[1]), pack2(yv[2], yv[3]), pack2(yv[4], yv[5]), pack2(yv[6], yv[7])));
+        }
     }
 }
 
