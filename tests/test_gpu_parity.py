@@ -400,3 +400,18 @@ def test_dynamic_conv_first_position_reads_only_its_own_block():
     for b in range(B):
         assert np.array_equal(got[b * T], c["x_prev"][b])
         assert np.array_equal(got[b * T + 1:(b + 1) * T], x[b * T:(b + 1) * T - 1])
+
+
+def test_dynamic_conv_unaligned_corrections():
+    """Corrections at a 4-byte (not 16-byte) address take the scalar staging path: same result."""
+    B, T, C, G = 2, 6, 256, 16
+    c = make_conv_inputs(B, T, C, G, seed=11)
+    d_al = dev(c["dyn"])
+    flat = torch.zeros(c["dyn"].size + 1, dtype=torch.float32, device="cuda")
+    flat[1:] = d_al.reshape(-1)
+    d_un = flat[1:].view(c["dyn"].shape)
+    assert d_un.data_ptr() % 16 != 0
+    args = dict(x_prev=dev_bf16(c["x_prev"]), gamma=dev_bf16(c["gamma"]), eps=1e-6, G=G)
+    y_al = df.dflash2_dynamic_conv(dev_bf16(c["x"]), dev_bf16(c["base"]), d_al, T, **args)
+    y_un = df.dflash2_dynamic_conv(dev_bf16(c["x"]), dev_bf16(c["base"]), d_un, T, **args)
+    assert torch.equal(y_al.view(torch.int16), y_un.view(torch.int16))
