@@ -17,8 +17,9 @@ constexpr int kWarps = kThreads / 32;
 
 // One CTA per (row, column slice), 8 warps.  Each warp keeps one warp-wide sorted list
 // (lane j holds entry j) over a contiguous part of the slice: lanes load 16-byte groups
-// (8 in flight per lane) and test them against the list's k-th entry, so only the rare
-// candidates that beat it are inserted (a per-thread list would diverge: some lane of the
+// (8 in flight per lane); a group of 128 values is offered to the list only when one of
+// them beats the list's k-th entry, which after the first few groups is rare, and then only
+// the lanes holding such values insert (a per-thread list would diverge: some lane of the
 // warp would insert on almost every step).  A bitonic butterfly then merges the 8 warp
 // lists into the slice's partial list.
 template <int KP, bool kVec4>
@@ -41,6 +42,7 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
         const int w1 = g0 + static_cast<int>(static_cast<long long>(warp + 1) * (g1 - g0) / kWarps);
         const float4 *row4 = reinterpret_cast<const float4 *>(row);
         constexpr int kU = 8;  // 16-byte loads in flight per lane
+        float thr = -INFINITY;  // value of the list's KP-th entry (warp-uniform)
         for (int g = w0 + lane; g < w1 + lane; g += 32 * kU) {
             float4 x[kU];
 #pragma unroll
@@ -50,11 +52,18 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
             }
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
-                const int gi = g + 32 * u;
-                wl.offer(x[u].x, 4 * gi, KP);
-                wl.offer(x[u].y, 4 * gi + 1, KP);
-                wl.offer(x[u].z, 4 * gi + 2, KP);
-                wl.offer(x[u].w, 4 * gi + 3, KP);
+                // Every id of this 128-value group is above every id already in the list, so
+                // a value equal to the KP-th entry ranks after it: only a strictly larger
+                // value can enter, and most groups have none.
+                const float m = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
+                if (__any_sync(kFullMask, m > thr)) {
+                    const int gi = g + 32 * u;
+                    wl.offer(x[u].x, 4 * gi, KP);
+                    wl.offer(x[u].y, 4 * gi + 1, KP);
+                    wl.offer(x[u].z, 4 * gi + 2, KP);
+                    wl.offer(x[u].w, 4 * gi + 3, KP);
+                    thr = __shfl_sync(kFullMask, wl.v, KP - 1);
+                }
             }
         }
     } else {
