@@ -245,6 +245,15 @@ DF2_API df2_status dflash2_dynamic_conv(const df2_conv_dims *dims, const void *x
  * check (the kernel then skipped its remaining work and its outputs are invalid). */
 DF2_API df2_status dflash2_check_device_status(void *workspace, size_t workspace_bytes, void *stream);
 
+/* Self-test of the device-side failure detection (no counterpart in the pages): one
+ * thread waits, through the bounded-wait helper that every pipeline wait of the LM-head
+ * kernel uses, on an mbarrier that nothing arrives on.  After limit_us microseconds
+ * (1 .. 1,000,000) the wait gives up and raises a bit of the workspace's status word, as a
+ * stalled pipeline would; dflash2_check_device_status then returns DF2_ERR_TIMEOUT (and
+ * clears the word).  Enqueued on `stream`; nothing else is touched. */
+DF2_API df2_status dflash2_selftest_wait_timeout(uint32_t limit_us, void *workspace, size_t workspace_bytes,
+                                                 void *stream);
+
 /* Timing hook: on this host thread, every following dflash2_select /
  * dflash2_select_from_logits call records `begin` on its stream just before the
  * LM-head (or logits top-k) launch and `end` just after it, so the caller can read

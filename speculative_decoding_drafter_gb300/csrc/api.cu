@@ -415,6 +415,18 @@ df2_status dflash2_check_device_status(void *workspace, size_t workspace_bytes, 
     return DF2_OK;
 }
 
+df2_status dflash2_selftest_wait_timeout(uint32_t limit_us, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (limit_us == 0 || limit_us > 1000000u)
+        return DF2_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < kAlign)
+        return DF2_ERR_WORKSPACE;
+    cudaGetLastError();
+    DF2_CUDA(launch_wait_selftest(static_cast<uint32_t *>(workspace), 1000ull * limit_us,
+                                  static_cast<cudaStream_t>(stream)));
+    return DF2_OK;
+}
+
 df2_status dflash2_profile_events(void *begin, void *end)
 {
     if ((begin == nullptr) != (end == nullptr))

@@ -65,4 +65,7 @@ cudaError_t launch_dynamic_conv(int B, int T, int C, int G, const uint16_t *x, c
 // Greedy walk, one warp per sequence: draft_ids [B, T].
 cudaError_t launch_walk(int B, int T, int k, const float *lattice, int32_t *draft_ids, cudaStream_t stream);
 
+// selftest.cu
+cudaError_t launch_wait_selftest(uint32_t *status, unsigned long long limit_ns, cudaStream_t stream);
+
 }  // namespace df2

@@ -9,6 +9,7 @@ namespace df2 {
 
 // Device status word bits (sticky; read by dflash2_check_device_status).
 constexpr uint32_t kStatusTimeoutGemm = 1u << 0;
+constexpr uint32_t kStatusTimeoutSelftest = 1u << 1;
 
 // A pipeline wait gives up after this long (a healthy call finishes in milliseconds).
 constexpr unsigned long long kWaitTimeoutNs = 1000000000ull;
@@ -61,9 +62,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Waits for the phase of parity `parity` to complete.  Gives up (returns false) when
-// another role of the CTA raised *abort, or after kWaitTimeoutNs, in which case it
-// raises *abort itself.  Every wait in the pipelined kernels goes through here.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort)
+// another role of the CTA raised *abort, or after limit_ns, in which case it raises
+// *abort itself.  Every wait in the pipelined kernels goes through here.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned long long limit_ns = kWaitTimeoutNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -74,7 +76,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if ((it & 63u) == 0u) {
             if (*abort)
                 return false;
-            if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }

@@ -23,7 +23,7 @@ __all__ = [
     "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
     "dflash2_profile_events", "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv",
     "ConvDims", "EXPORTED_SYMBOLS", "dflash2_select_host", "dflash2_select_host_workspace_bytes", "HostWorkspace",
-    "SelectHostPlan",
+    "SelectHostPlan", "dflash2_selftest_wait_timeout",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
     "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
     "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv", "dflash2_select_host",
-    "dflash2_select_host_workspace_bytes",
+    "dflash2_select_host_workspace_bytes", "dflash2_selftest_wait_timeout",
 )
 
 
@@ -88,6 +88,7 @@ def library(path: str | None = None):
                 "dflash2_dynamic_conv": (I, [ctypes.POINTER(ConvDims), P, P, P, P, P, ctypes.c_float, P, P]),
                 "dflash2_select_host": (I, [D, P, P, P, P, P, P, P, P, P, S, P]),
                 "dflash2_select_host_workspace_bytes": (S, [D]),
+                "dflash2_selftest_wait_timeout": (I, [ctypes.c_uint32, P, S, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -456,6 +457,13 @@ def dflash2_check_device_status(workspace: Workspace, stream=None) -> None:
     """Synchronises the stream; raises DFlash2Error(DF2_ERR_TIMEOUT) if a kernel wait gave up."""
     _check(library().dflash2_check_device_status(workspace.ptr, workspace.nbytes, _stream(stream)),
            "dflash2_check_device_status")
+
+
+def dflash2_selftest_wait_timeout(workspace: Workspace, limit_us: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test: a device wait that nothing satisfies gives up after
+    limit_us and raises the workspace's status word (read it with dflash2_check_device_status)."""
+    _check(library().dflash2_selftest_wait_timeout(int(limit_us), workspace.ptr, workspace.nbytes, _stream(stream)),
+           "dflash2_selftest_wait_timeout")
 
 
 def dflash2_profile_events(begin=None, end=None) -> None:

@@ -145,3 +145,10 @@ def test_select_host_workspace_and_rejections(lib):
     assert call(dd=dims(k=0)) == DF2_ERR_INVALID_ARG
     assert call(ws_bytes=base) == DF2_ERR_WORKSPACE  # room for dflash2_select only, not the staging
     assert call(ws=0x100010) == DF2_ERR_WORKSPACE
+
+
+def test_selftest_wait_timeout_rejections(lib):
+    assert lib.dflash2_selftest_wait_timeout(0, 0x100000, 4096, None) == DF2_ERR_INVALID_ARG
+    assert lib.dflash2_selftest_wait_timeout(1000001, 0x100000, 4096, None) == DF2_ERR_INVALID_ARG
+    assert lib.dflash2_selftest_wait_timeout(100, None, 4096, None) == DF2_ERR_WORKSPACE
+    assert lib.dflash2_selftest_wait_timeout(100, 0x100010, 4096, None) == DF2_ERR_WORKSPACE
