@@ -78,9 +78,10 @@ Workspace carve(const df2_dims &d, void *base)
     w.counters = reinterpret_cast<unsigned *>(p ? p + off : nullptr);
     off += round_up(sizeof(unsigned) * static_cast<size_t>(d.B));
     w.pval = reinterpret_cast<float *>(p ? p + off : nullptr);
-    off += round_up(R * kMaxSplits * kp * sizeof(float));
+    const size_t splits = static_cast<size_t>(max_splits_for(static_cast<long long>(R)));
+    off += round_up(R * splits * kp * sizeof(float));
     w.pid = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
-    off += round_up(R * kMaxSplits * kp * sizeof(int32_t));
+    off += round_up(R * splits * kp * sizeof(int32_t));
     w.best = reinterpret_cast<int32_t *>(p ? p + off : nullptr);
     off += round_up(R * d.k * sizeof(int32_t));
     w.gate = reinterpret_cast<float *>(p ? p + off : nullptr);

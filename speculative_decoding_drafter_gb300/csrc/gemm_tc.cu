@@ -441,7 +441,7 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     args.n_store = n_store;
     const int units = (args.n_topk_pad + n_store + UNIT - 1) / UNIT;
     args.row_tiles = (R + BM - 1) / BM;
-    args.n_split = std::max(1, std::min({kMaxSplits, units, std::max(1, sms / args.row_tiles)}));
+    args.n_split = std::max(1, std::min({max_splits_for(R), units, std::max(1, sms / args.row_tiles)}));
     if (n_split_out)
         *n_split_out = args.n_split;
     const dim3 grid(static_cast<unsigned>(args.row_tiles * args.n_split));

@@ -11,6 +11,15 @@ namespace df2 {
 // Partial top-k lists hold at most this many vocabulary splits per row.
 constexpr int kMaxSplits = 256;
 
+// Splits per row that a launch over R rows may use, whatever the device: the LM head makes
+// about SMs / ceil(R / 128) column slices and the top-k of given logits about 4 * SMs / R,
+// so with at most 1024 SMs neither exceeds ceil(131072 / R).  Workspaces are sized by it.
+inline int max_splits_for(long long R)
+{
+    const long long b = R > 0 ? (131072 + R - 1) / R : 1;
+    return static_cast<int>(b < 1 ? 1 : b > kMaxSplits ? kMaxSplits : b);
+}
+
 // Capacity of the per-row candidate lists for a requested k (4, 8, 16 or 32).
 inline int kp_for(int k) { return k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32; }
 

@@ -136,7 +136,7 @@ cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32
     // about four CTAs per SM in total, slices of at least 2048 columns
     const int sms = device_sm_count();
     int n_split = std::max(1, (4 * sms + R - 1) / R);
-    n_split = std::min({n_split, kMaxSplits, std::max(1, V / 2048)});
+    n_split = std::min({n_split, max_splits_for(R), std::max(1, V / 2048)});
     *n_split_out = n_split;
     const dim3 grid(static_cast<unsigned>(R), static_cast<unsigned>(n_split));
     const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);

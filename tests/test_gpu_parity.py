@@ -276,6 +276,43 @@ def test_select_edge_shapes(B, T, H, V, k, D):
     assert compared + low >= 1
 
 
+def test_select_largest_vocabulary():
+    """V = 2^24 - 1, the largest vocabulary whose ids are exact in the float32 lattice, with k = 32."""
+    B, T, H, V, k, D = 1, 2, 8, (1 << 24) - 1, 32, 8
+    cfg, x = small_case(B, T, H, V, k, D, seed=3)
+    x["W_vocab"][V - 1] = x["hidden"][0]  # logit |h_0|^2, far above the ~5.6 sigma maximum of the rest
+    lat, draft = run_select(x, cfg)
+    assert int(lat[0, 0]) == V - 1 and lat[0, 0] == np.float32(V - 1)
+    ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
+    tol = row_tol(ora["logits"])
+    ids = lat[:, :k].astype(np.int32)
+    check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+                           ora["topk_vals"], tol)
+    compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
+    assert compared + low >= 1
+
+
+def test_select_most_rows():
+    """B*T = 2^20 rows, the row limit: 8192 row tiles in the LM head, 2^20 CTAs in the finish kernel."""
+    B, T, H, V, k, D = 65536, 16, 8, 64, 4, 8
+    cfg, x = small_case(B, T, H, V, k, D, seed=4)
+    lat, draft = run_select(x, cfg)
+    assert lat.shape == (B * T, k + k * k) and draft.shape == (B, T)
+    total = 0
+    for b in (0, 31337, B - 1):
+        rows = np.arange(b * T, (b + 1) * T)
+        ora = oracle.select(x["hidden"][rows], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"],
+                            x["anchor"][b:b + 1], k, T)
+        tol = row_tol(ora["logits"])
+        ids = lat[rows, :k].astype(np.int32)
+        check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+                               ora["topk_vals"], tol)
+        compared, low = compare_lattice_and_draft(lat[rows], draft[b:b + 1], ora, T, k, tol)
+        assert compared + low >= 1
+        total += compared
+    assert total >= T, f"only {total} of {3 * T} draft steps were comparable"
+
+
 def test_zeroed_codebooks_give_per_position_top1():
     cfg, x = small_case(4, 6, 256, 2048, 8, 32, seed=5)
     x["pred_cb"][:] = 0
