@@ -201,8 +201,20 @@ def cpu_baseline(cfg, x, budget_s: float = 20.0):
     t_row = time_oracle_rows(cfg, x, 1, 0)
     n_rows = int(max(1, min(cfg.T, budget_s / max(t_row, 1e-9))))
     t = time_oracle_rows(cfg, x, n_rows, 0)
-    return {"value": n_rows / t, "unit": "rows/s", "cores": oracle.threads(), "kind": "oracle",
+    line = {"value": n_rows / t, "unit": "rows/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"sequence 0, positions 0..{n_rows - 1} of {cfg.T} (full vocabulary, full pipeline), one run"}
+    # the same oracle on one core, on as many rows as fit a quarter of the budget
+    prev = oracle.set_threads(1)
+    try:
+        t1 = time_oracle_rows(cfg, x, 1, 0)
+        n1 = int(max(1, min(cfg.T, 0.25 * budget_s / max(t1, 1e-9))))
+        if n1 > 1:
+            t1 = time_oracle_rows(cfg, x, n1, 0)
+    finally:
+        oracle.set_threads(prev)
+    line["value_1_thread"] = n1 / t1
+    line["sample_1_thread"] = f"sequence 0, positions 0..{n1 - 1}, one thread"
+    return line
 
 
 def run_reference(args, cfg, rank: int):
@@ -301,6 +313,11 @@ def run_ours(args, cfg, rank: int, world: int):
     df.dflash2_check_device_status(ws)
     ms = max_over_ranks(start.elapsed_time(end), dist, "cuda")
     lm_ms = sum(eb[i].elapsed_time(ee[i]) for i in range(K)) / K
+    # per-step spread: a step runs from one LM-head launch to the next (the last to the end event)
+    step_us = [1e3 * eb[i].elapsed_time(eb[i + 1]) for i in range(K - 1)] + [1e3 * eb[K - 1].elapsed_time(end)]
+    lm_us = [1e3 * eb[i].elapsed_time(ee[i]) for i in range(K)]
+    pct = {name: {f"p{q}": float(np.percentile(v, q)) for q in (10, 50, 90)}
+           for name, v in (("step_us", step_us), ("lm_head_us", lm_us))}
 
     # ---- end-to-end through the C ABI's host-buffer call (pinned buffers): every step copies
     # hidden and anchor in and the draft, lattice and status word out, and waits for them
@@ -363,6 +380,7 @@ def run_ours(args, cfg, rank: int, world: int):
                    if cfg.V * cfg.H * 2 > 129e6 else "inputs fit in L2 (warm)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
+        "percentiles": pct,
         "gpu_launches": LAUNCHES_PER_STEP * K,
         "clocks": clocks,
         "e2e": e2e,

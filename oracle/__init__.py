@@ -73,10 +73,11 @@ def _load():
         lib.oracle_lattice.argtypes = [i64, i64, i32, i64, i64, p, p, p, p, p, p, p, p]
         lib.oracle_walk.argtypes = [i64, i64, i32, p, p, p]
         lib.oracle_threads.argtypes = []
+        lib.oracle_set_threads.argtypes = [i32]
         lib.oracle_walk_sample.argtypes = [i64, i64, i32, p, ctypes.c_double, ctypes.c_double, p, p, p, p]
         lib.oracle_dynamic_conv.argtypes = [i64, i64, i64, i64, p, p, p, p, p, ctypes.c_double, p]
         for f in (lib.oracle_logits, lib.oracle_topk, lib.oracle_gate, lib.oracle_lattice, lib.oracle_walk,
-                  lib.oracle_threads, lib.oracle_walk_sample, lib.oracle_dynamic_conv):
+                  lib.oracle_threads, lib.oracle_walk_sample, lib.oracle_dynamic_conv, lib.oracle_set_threads):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -85,6 +86,11 @@ def _load():
 def threads() -> int:
     """OpenMP threads the oracle's loops use."""
     return int(_load().oracle_threads())
+
+
+def set_threads(n: int) -> int:
+    """Use n OpenMP threads from now on; returns the previous count."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 def _ptr(a):

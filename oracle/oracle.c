@@ -70,6 +70,20 @@ int oracle_threads(void)
 #endif
 }
 
+/* Threads for the following calls (n >= 1); returns the previous count.  Only the
+ * baseline timing uses it, to time the oracle on one core as well as on all of them. */
+int oracle_set_threads(int n)
+{
+    const int prev = oracle_threads();
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return prev;
+}
+
 static double bf16_to_double(uint16_t bits)
 {
     uint32_t u = ((uint32_t)bits) << 16;
