@@ -42,7 +42,8 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
         const int w1 = g0 + static_cast<int>(static_cast<long long>(warp + 1) * (g1 - g0) / kWarps);
         const float4 *row4 = reinterpret_cast<const float4 *>(row);
         constexpr int kU = 8;  // 16-byte loads in flight per lane
-        float thr = -INFINITY;  // value of the list's KP-th entry (warp-uniform)
+        float thr = -INFINITY;  // the list's KP-th entry (warp-uniform)
+        int thr_i = INT_MAX;
         for (int g = w0 + lane; g < w1 + lane; g += 32 * kU) {
             float4 x[kU];
 #pragma unroll
@@ -57,12 +58,25 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
                 // value can enter, and most groups have none.
                 const float m = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
                 if (__any_sync(kFullMask, m > thr)) {
-                    const int gi = g + 32 * u;
-                    wl.offer(x[u].x, 4 * gi, KP);
-                    wl.offer(x[u].y, 4 * gi + 1, KP);
-                    wl.offer(x[u].z, 4 * gi + 2, KP);
-                    wl.offer(x[u].w, 4 * gi + 3, KP);
-                    thr = __shfl_sync(kFullMask, wl.v, KP - 1);
+                    // ids of the group: 4 * (base + lane) + component, base warp-uniform
+                    const int base = g - lane + 32 * u;
+                    const float xc[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        // >= keeps every value that may enter; ranks_before decides exactly
+                        unsigned cand = __ballot_sync(kFullMask, xc[c] >= thr);
+                        while (cand) {
+                            const int src = __ffs(cand) - 1;
+                            cand &= cand - 1u;
+                            const float cv = __shfl_sync(kFullMask, xc[c], src);
+                            const int ci = 4 * (base + src) + c;
+                            if (ranks_before(cv, ci, thr, thr_i)) {
+                                wl.insert(cv, ci);
+                                thr = __shfl_sync(kFullMask, wl.v, KP - 1);
+                                thr_i = __shfl_sync(kFullMask, wl.i, KP - 1);
+                            }
+                        }
+                    }
                 }
             }
         }
