@@ -47,7 +47,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="8b_b1", choices=list(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--op", default="select", choices=["select", "conv", "topk"],
+    ap.add_argument("--op", default="select", choices=["select", "conv", "topk", "walk"],
                     help="select: the selector head (default); conv: the dynamic local convolution; "
                          "topk: top-k A/B (fused epilogue vs materialised logits, ours vs torch.topk)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed oracle sample")
@@ -486,6 +486,115 @@ def run_conv(args, rank: int, world: int):
     return 0
 
 
+WALK_SHAPE = (8192, 16, 16)  # sequences, positions, candidates: a 143 MB lattice, larger than L2
+
+
+def run_walk(args, rank: int, world: int):
+    """The walk with confidence, p_min stop and inverse-CDF sampling (and the plain greedy walk) over a
+    seeded lattice of WALK_SHAPE.  One warp per sequence, T dependent row reads: latency-bound."""
+    import torch
+
+    from speculative_decoding_drafter_gb300 import dflash2 as df
+
+    if rank != 0:
+        return 0
+    B, T, k = WALK_SHAPE
+    R, W = B * T, k + k * k
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([0, 41])))
+    lat = np.empty((R, W), np.float32)
+    lat[:, :k] = g.integers(0, 151936, size=(R, k))
+    lat[:, k:] = (1.5 * g.standard_normal((R, k * k))).astype(np.float32)
+    uni = g.random((B, T), dtype=np.float32)
+    tau, p_min = 1.0, 0.3
+    name = f"walk: B={B} T={T} k={k}, temperature {tau}, p_min {p_min}, sampling with given uniforms"
+    # bytes a walk must touch: per position the chosen predecessor row (k floats), the chosen id, the
+    # uniform, and the draft and confidence it writes; plus n_draft per sequence
+    algo = R * (k * 4 + 4 + 4 + 4 + 4) + B * 4
+    sample_b = 256
+    if args.impl == "reference":
+        import oracle
+
+        oracle.build()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.walk_sample(lat[:sample_b * T], sample_b, T, k, tau, p_min, uni[:sample_b])
+        dt = time.perf_counter() - t0
+        v = sample_b * args.steps / dt
+        print(json.dumps({"impl": "reference", "op": "walk", "metric": "sampling walk sequences/s", "value": v,
+                          "unit": "sequences/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                          "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+                          "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": {"workload": name},
+                          "cpu_baseline": {"value": v, "unit": "sequences/s", "cores": oracle.threads(),
+                                           "kind": "oracle", "sample": f"{sample_b} sequences per step"},
+                          "e2e": {"value": v, "unit": "sequences/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    peaks, peak_kind = load_peaks()
+    d_lat = torch.from_numpy(lat).cuda()
+    d_uni = torch.from_numpy(uni).cuda()
+    draft = torch.empty((B, T), dtype=torch.int32, device="cuda")
+    n_draft = torch.empty((B,), dtype=torch.int32, device="cuda")
+    conf = torch.empty((B, T), dtype=torch.float32, device="cuda")
+
+    def sampled():
+        df.dflash2_walk_sample(d_lat, B, T, k, temperature=tau, p_min=p_min, uniforms=d_uni, draft=draft,
+                               n_draft=n_draft, confidence=conf)
+
+    def greedy():
+        df.dflash2_walk(d_lat, B, T, k, out=draft)
+
+    # the walk touches only the rows it chooses (~10 MB), the same ones every call: flush L2 before each
+    # timed launch by writing a buffer twice its size, outside the launch's own event pair
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed(f):
+        for _ in range(args.warmup):
+            f()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record()
+            f()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / args.steps * 1e3
+
+    sampler = ClockSampler(device_id_for_smi(torch))
+    sampler.start()
+    us = timed(sampled)
+    clock_rows = sampler.stop()
+    greedy_us = timed(greedy)
+    sampled()
+    torch.cuda.synchronize()
+    o_draft, o_n, o_conf = oracle_walk_sample_sample(lat, uni, sample_b, T, k, tau, p_min)
+    g_draft, g_n = draft.cpu().numpy()[:sample_b], n_draft.cpu().numpy()[:sample_b]
+    agree = float(np.mean(np.all(g_draft == o_draft, axis=1) & (g_n == o_n)))
+    achieved = algo / (us / 1e6) / 1e9
+    print(json.dumps({
+        "impl": "ours", "op": "walk", "metric": "sampling walk sequences/s", "value": B / (us / 1e6),
+        "unit": "sequences/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": name, "l2": "flushed before every timed launch (256 MB write, outside the timing)"},
+        "greedy_walk_us": greedy_us, "sampling_walk_us": us,
+        "sample_agreement_with_oracle": agree, "agreement_sample": f"first {sample_b} sequences, exact draft and n_draft",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "walk_sample_kernel",
+                     "algorithmic_per_launch": algo, "peak_source": peak_kind,
+                     "note": "latency-bound: T dependent row reads per sequence"},
+        "gpu_launches": args.steps,
+        "clocks": ClockSampler.summarize(clock_rows, 0) if clock_rows else {"reasons": ["no samples"]}}), flush=True)
+    return 0
+
+
+def oracle_walk_sample_sample(lat, uni, nb, T, k, tau, p_min):
+    """The oracle's walk on the first nb sequences (the bench's parity spot check)."""
+    import oracle
+
+    return oracle.walk_sample(lat[:nb * T], nb, T, k, tau, p_min, uni[:nb])
+
+
 def run_topk(args, cfg, rank: int):
     """Top-k A/B on one config: (a) dflash2_topk vs torch.topk over the same materialised float32
     logits; (b) the fused LM head (top-k in the epilogue) vs materialising the logits and then
@@ -577,6 +686,8 @@ def main():
         return run_conv(args, rank, world)
     if args.op == "topk":
         return run_topk(args, cfg, rank)
+    if args.op == "walk":
+        return run_walk(args, rank, world)
     if args.impl == "reference":
         return run_reference(args, cfg, rank)
     return run_ours(args, cfg, rank, world)
