@@ -152,3 +152,24 @@ def test_selftest_wait_timeout_rejections(lib):
     assert lib.dflash2_selftest_wait_timeout(1000001, 0x100000, 4096, None) == DF2_ERR_INVALID_ARG
     assert lib.dflash2_selftest_wait_timeout(100, None, 4096, None) == DF2_ERR_WORKSPACE
     assert lib.dflash2_selftest_wait_timeout(100, 0x100010, 4096, None) == DF2_ERR_WORKSPACE
+
+
+def test_header_is_usable_from_plain_c(lib, tmp_path):
+    """include/dflash2.h compiles as C99 and the library links and answers from a C program."""
+    import shutil
+    import subprocess
+
+    from speculative_decoding_drafter_gb300.build import LIB_PATH
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    exe = tmp_path / "abi_from_c"
+    libdir = os.path.dirname(LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"),
+                    os.path.join(root, "tests", "c", "abi_from_c.c"), "-o", str(exe), "-L", libdir, "-ldflash2",
+                    "-Wl,-rpath," + libdir], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "ok"
