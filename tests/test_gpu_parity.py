@@ -452,3 +452,52 @@ def test_dynamic_conv_unaligned_corrections():
     y_al = df.dflash2_dynamic_conv(dev_bf16(c["x"]), dev_bf16(c["base"]), d_al, T, **args)
     y_un = df.dflash2_dynamic_conv(dev_bf16(c["x"]), dev_bf16(c["base"]), d_un, T, **args)
     assert torch.equal(y_al.view(torch.int16), y_un.view(torch.int16))
+
+
+def _random_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        k = int(rng.integers(1, 33))
+        out.append((int(rng.integers(1, 7)), int(rng.integers(1, 18)), 8 * int(rng.integers(1, 129)),
+                    int(rng.integers(k, 20001)), k, 8 * int(rng.integers(1, 33))))
+    return out
+
+
+@pytest.mark.parametrize("B,T,H,V,k,D", _random_shapes(24, 2024))
+def test_select_random_shapes(B, T, H, V, k, D):
+    """Seeded random shapes across the limits: the fused path against the oracle under the same rules."""
+    cfg, x = small_case(B, T, H, V, k, D, seed=B * 1000 + T * 10 + k)
+    lat, draft = run_select(x, cfg)
+    ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
+    tol = row_tol(ora["logits"])
+    ids = lat[:, :k].astype(np.int32)
+    swaps = check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+                                   ora["topk_vals"], tol)
+    assert swaps <= max(1, (B * T) // 20)
+    compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
+    assert compared + low >= 1
+
+
+def _random_conv_shapes(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        G = 8 * int(rng.integers(1, 5))
+        out.append((int(rng.integers(1, 9)), int(rng.integers(1, 20)), G * int(rng.integers(1, 65)), G,
+                    bool(rng.integers(0, 2)), bool(rng.integers(0, 2))))
+    return out
+
+
+@pytest.mark.parametrize("B,T,C,G,prev,norm", _random_conv_shapes(16, 7))
+def test_dynamic_conv_random_shapes(B, T, C, G, prev, norm):
+    c = make_conv_inputs(B, T, C, G, seed=B * 100 + T + C)
+    xp = c["x_prev"] if prev else None
+    gm = c["gamma"] if norm else None
+    y = df.dflash2_dynamic_conv(dev_bf16(c["x"]), dev_bf16(c["base"]), dev(c["dyn"]), T,
+                                x_prev=None if xp is None else dev_bf16(xp), gamma=None if gm is None else dev_bf16(gm),
+                                eps=1e-6, G=G)
+    got = bf16_bits_to_f32(host(y.view(torch.int16)).view(np.uint16)).astype(np.float64)
+    ref = oracle.dynamic_conv(c["x"], xp, c["base"], c["dyn"], T, G, gamma=gm, eps=1e-6)
+    err = np.abs(got - ref)
+    assert np.all(err <= _conv_tol(ref)), f"max excess {(err - _conv_tol(ref)).max()}"
