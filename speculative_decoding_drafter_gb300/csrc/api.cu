@@ -237,21 +237,36 @@ df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, co
     if (!workspace || !aligned(workspace, kAlign) || workspace_bytes < carve_staging(d, nullptr).bytes)
         return DF2_ERR_WORKSPACE;
     const Staging s = carve_staging(d, workspace);
+    // every check dflash2_select makes, before anything is enqueued
+    DF2_TRY(check_tail_pointers(W_sel, pred_cb, succ_cb, s.anchor, s.lattice, s.draft, nullptr, nullptr, nullptr));
     const size_t R = static_cast<size_t>(d.B) * d.T;
     const size_t width = static_cast<size_t>(d.k) + static_cast<size_t>(d.k) * d.k;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaGetLastError();
-    DF2_CUDA(cudaMemcpyAsync(s.hidden, hidden_host, R * d.H * sizeof(uint16_t), cudaMemcpyHostToDevice, st));
-    DF2_CUDA(cudaMemcpyAsync(s.anchor, anchor_host, d.B * sizeof(int32_t), cudaMemcpyHostToDevice, st));
-    DF2_TRY(dflash2_select(dims, s.hidden, W_vocab, W_sel, pred_cb, succ_cb, s.anchor, s.lattice, s.draft, nullptr,
-                           nullptr, nullptr, workspace, workspace_bytes, stream));
-    DF2_CUDA(cudaMemcpyAsync(draft_ids_host, s.draft, R * sizeof(int32_t), cudaMemcpyDeviceToHost, st));
-    if (lattice_host)
-        DF2_CUDA(cudaMemcpyAsync(lattice_host, s.lattice, R * width * sizeof(float), cudaMemcpyDeviceToHost, st));
+    // once work is enqueued, a failure still waits for the stream: no copy from or to the
+    // caller's host buffers may be in flight when the call returns
+    auto fail = [&](df2_status e) {
+        cudaStreamSynchronize(st);
+        return e;
+    };
+    if (cudaMemcpyAsync(s.hidden, hidden_host, R * d.H * sizeof(uint16_t), cudaMemcpyHostToDevice, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(s.anchor, anchor_host, d.B * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return fail(DF2_ERR_CUDA);
+    const df2_status e = dflash2_select(dims, s.hidden, W_vocab, W_sel, pred_cb, succ_cb, s.anchor, s.lattice,
+                                        s.draft, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream);
+    if (e != DF2_OK)
+        return fail(e);
+    if (cudaMemcpyAsync(draft_ids_host, s.draft, R * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        (lattice_host &&
+         cudaMemcpyAsync(lattice_host, s.lattice, R * width * sizeof(float), cudaMemcpyDeviceToHost, st) !=
+             cudaSuccess))
+        return fail(DF2_ERR_CUDA);
     // The status word comes back behind the results; a stack destination is pageable
     // memory, for which the copy returns only once it is complete.
     uint32_t word = 0;
-    DF2_CUDA(cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st));
+    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return fail(DF2_ERR_CUDA);
     DF2_CUDA(cudaStreamSynchronize(st));
     return word == 0 ? DF2_OK : DF2_ERR_TIMEOUT;
 }

@@ -145,6 +145,9 @@ def test_select_host_workspace_and_rejections(lib):
     assert call(dd=dims(k=0)) == DF2_ERR_INVALID_ARG
     assert call(ws_bytes=base) == DF2_ERR_WORKSPACE  # room for dflash2_select only, not the staging
     assert call(ws=0x100010) == DF2_ERR_WORKSPACE
+    # device pointers are checked before any copy is enqueued (W_sel not 16-byte aligned)
+    assert lib.dflash2_select_host(ctypes.byref(d), h, w, w + 8, w, w, a, lat, dr, 0x100000, n, None) == \
+        DF2_ERR_INVALID_ARG
 
 
 def test_selftest_wait_timeout_rejections(lib):
