@@ -29,6 +29,31 @@ int device_sm_count()
     return cache[dev];
 }
 
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes)
+{
+    struct Entry {
+        const void *kernel;
+        int dev, bytes;
+    };
+    constexpr int kEntries = 32;
+    thread_local Entry seen[kEntries];
+    thread_local int used = 0, next = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    for (int i = 0; i < used; ++i)
+        if (seen[i].kernel == kernel && seen[i].dev == dev && seen[i].bytes >= bytes)
+            return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess)
+        return e;
+    seen[next] = Entry{kernel, dev, bytes};
+    next = (next + 1) % kEntries;
+    used = used < kEntries ? used + 1 : kEntries;
+    return cudaSuccess;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;

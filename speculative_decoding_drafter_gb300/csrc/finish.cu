@@ -181,8 +181,7 @@ cudaError_t launch_kp(FinishArgs a, int B, cudaStream_t stream)
     size_t smem = lattice_smem_bytes(a.k, a.D);
     if (a.walk_in_smem && walk_bytes > smem)
         smem = walk_bytes;
-    cudaError_t e = cudaFuncSetAttribute(finish_kernel<KP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(finish_kernel<KP>), static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};

@@ -382,7 +382,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // Row-major bf16 [rows, K] tensor, boxes of 64 K-elements x box_rows rows, 128-byte swizzle.
-cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows)
+cudaError_t encode_map(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows)
 {
     auto encode = tensor_map_encoder();
     if (!encode)
@@ -395,6 +395,34 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box
                               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// A map is a pure function of its encode parameters, so a drafting loop that calls with the
+// same buffers every step reuses the encodings (a small per-thread cache, oldest entry out).
+cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows)
+{
+    struct Entry {
+        const void *ptr;
+        int K, rows, box_rows;
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 16;
+    thread_local Entry cache[kEntries];
+    thread_local int used = 0, next = 0;
+    for (int i = 0; i < used; ++i) {
+        const Entry &e = cache[i];
+        if (e.ptr == ptr && e.K == K && e.rows == rows && e.box_rows == box_rows) {
+            *map = e.map;
+            return cudaSuccess;
+        }
+    }
+    const cudaError_t err = encode_map(map, ptr, K, rows, box_rows);
+    if (err != cudaSuccess)
+        return err;
+    cache[next] = Entry{ptr, K, rows, box_rows, *map};
+    next = (next + 1) % kEntries;
+    used = used < kEntries ? used + 1 : kEntries;
+    return cudaSuccess;
 }
 
 template <int KP>
@@ -431,7 +459,7 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
         (e = make_map(&msw, sb, K, sn, args.bn)) != cudaSuccess || (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
         return e;
     auto kern = gemm_tc_kernel<KP>;
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess)
+    if ((e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem_bytes)) != cudaSuccess)
         return e;
     const int sms = device_sm_count();
     args.R = R;

@@ -26,6 +26,10 @@ inline int kp_for(int k) { return k <= 4 ? 4 : k <= 8 ? 8 : k <= 16 ? 16 : 32; }
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
+// Opts `kernel` in to at least `bytes` of dynamic shared memory on the current device; the
+// attribute is set once per kernel, device and size (remembered per host thread).
+cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
+
 // LM head (and gate) in one tensor-core launch: C = hidden[R, K] . [W_vocab; W_store]^T
 // (bf16 in, float32 accumulate).  The first V columns are reduced on the fly to per-row
 // top-KP lists over each CTA's column slice, pval/pid [R, n_split, KP] (value desc, id
