@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---------------- TMA producer
+            const uint64_t stream_policy = l2_policy_evict_first();
             int stage = 0;
             uint32_t phase = 0;
             long long issued = 0;
@@ -215,11 +216,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const int x = (ks * kbs + q) * BK;  // past K the boxes read zeros
                         tma_load_2d(smem_u32(st + q * args.a_bytes), &map_a, full_bar(stage), x, m_tile * BM);
                         const uint32_t b_dst = smem_u32(st + kbs * args.a_bytes + q * b_sub);
+                        // the weights stream through once: evict-first in L2 (measured on GB300:
+                        // 197.3 vs 198.0 us at 16 rows, 248.3 vs 250.0 at 64, 449.9 vs 455.1 at 512)
                         if (ch.n == args.bn) {
-                            tma_load_2d(b_dst, wide, full_bar(stage), x, ch.b_row);
+                            tma_load_2d_policy(b_dst, wide, full_bar(stage), x, ch.b_row, stream_policy);
                         } else {
                             for (int u = 0; u < ch.n / UNIT; ++u)
-                                tma_load_2d(b_dst + u * UNIT * BK * 2, narrow, full_bar(stage), x, ch.b_row + u * UNIT);
+                                tma_load_2d_policy(b_dst + u * UNIT * BK * 2, narrow, full_bar(stage), x,
+                                                   ch.b_row + u * UNIT, stream_policy);
                         }
                     }
                     ++issued;

@@ -109,6 +109,26 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map)
 
 // 2-D tiled load (x = innermost element coordinate, y = row) into shared memory,
 // completing `bytes` of transaction count on `bar`.  x * 2 bytes must be a multiple of 16.
+// L2 policy for data read once in a stream: its lines are the first to go when L2 needs room,
+// so what is re-read (the hidden-state tile, partial lists, gathers) stays resident.
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_2d with an L2 cache policy for the source lines.
+__device__ __forceinline__ void tma_load_2d_policy(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
+                                                   uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)
 {
     asm volatile(
