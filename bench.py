@@ -605,6 +605,28 @@ def run_topk(args, cfg, rank: int):
 
     if rank != 0:
         return 0
+    if args.impl == "reference":
+        # the oracle's top-k (a full sort per row) on a bounded sample of rows of seeded float32 logits
+        import oracle
+
+        oracle.build()
+        rows = 4
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([0, 43])))
+        lg = g.standard_normal((rows, cfg.V), dtype=np.float32)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle.topk(lg, cfg.k)
+        dt = (time.perf_counter() - t0) / args.steps
+        print(json.dumps({"impl": "reference", "op": "topk", "metric": "top-k of materialised float32 logits, us per call",
+                          "value": 1e6 * dt * cfg.R / rows, "unit": "us", "higher_is_better": False,
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "dtype": "f32",
+                          "data": "synthetic", "config": {"workload": workload_name(cfg)},
+                          "cpu_baseline": {"value": 1e6 * dt * cfg.R / rows, "unit": "us", "cores": oracle.threads(),
+                                           "kind": "oracle",
+                                           "sample": f"{rows} rows per step, scaled to the workload's {cfg.R} rows"},
+                          "e2e": {"value": 1e6 * dt * cfg.R / rows, "unit": "us", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
     torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
     peaks, peak_kind = load_peaks()
     R, V, H, k = cfg.R, cfg.V, cfg.H, cfg.k
