@@ -313,6 +313,28 @@ def test_select_most_rows():
     assert total >= T, f"only {total} of {3 * T} draft steps were comparable"
 
 
+def test_select_long_sequence_walks_from_global_memory():
+    """T * k above 8192: the finish kernel's walk reads its choice table from global memory."""
+    B, T, H, V, k, D = 2, 300, 64, 5000, 32, 16
+    cfg, x = small_case(B, T, H, V, k, D, seed=13)
+    lat, draft = run_select(x, cfg)
+    ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
+    tol = row_tol(ora["logits"])
+    ids = lat[:, :k].astype(np.int32)
+    check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+                           ora["topk_vals"], tol)
+    compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
+    assert compared + low >= 1
+    # the walk follows the lattice the kernel wrote, step by step, whatever the oracle's margins
+    for b in range(B):
+        j = 0
+        for t in range(T):
+            row = lat[b * T + t]
+            scores = row[k + j * k:k + (j + 1) * k]
+            j = int(np.argmax(scores))  # first maximum
+            assert draft[b, t] == int(row[j]), f"sequence {b} position {t}"
+
+
 def test_zeroed_codebooks_give_per_position_top1():
     cfg, x = small_case(4, 6, 256, 2048, 8, 32, seed=5)
     x["pred_cb"][:] = 0
