@@ -122,6 +122,32 @@ def test_select_is_deterministic(case):
     assert np.array_equal(host(draft), case["draft"])
 
 
+def test_select_properties_on_every_row(case):
+    """Checks that need no oracle, on every row of the full-size call."""
+    cfg = case["cfg"]
+    k, T, V = cfg.k, cfg.T, cfg.V
+    lat, draft, ids, vals = case["lat"], case["draft"], case["ids"], case["vals"]
+    R = cfg.R
+    # candidate ids: exact, in range, distinct within a row, equal to the packed ids
+    assert np.all((ids >= 0) & (ids < V))
+    assert np.all(np.sort(ids, axis=1)[:, 1:] != np.sort(ids, axis=1)[:, :-1])
+    assert np.array_equal(lat[:, :k], ids.astype(np.float32))
+    # unary scores sorted by (value desc, id asc)
+    v0, v1, i0, i1 = vals[:, :-1], vals[:, 1:], ids[:, :-1], ids[:, 1:]
+    assert np.all((v0 > v1) | ((v0 == v1) & (i0 < i1)))
+    assert np.all(np.isfinite(lat))
+    # position 0: every predecessor row holds the anchor-conditioned scores
+    s = lat[:, k:].reshape(R, k, k)
+    first = np.arange(0, R, T)
+    assert np.all(s[first] == s[first][:, :1, :])
+    # the draft is the greedy walk over the lattice the kernel wrote (first maximum)
+    sb = s.reshape(cfg.B, T, k, k)
+    j = np.zeros(cfg.B, dtype=np.int64)
+    for t in range(T):
+        j = np.argmax(sb[np.arange(cfg.B), t, j, :], axis=1)
+        assert np.array_equal(draft[:, t], ids.reshape(cfg.B, T, k)[np.arange(cfg.B), t, j]), f"position {t}"
+
+
 def test_select_host_matches_the_device_path(case):
     """Host buffers in and out: the same kernels on staged copies, so the same bits."""
     cfg, x, d = case["cfg"], case["x"], case["d"]
