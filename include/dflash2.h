@@ -146,6 +146,9 @@ DF2_API df2_status dflash2_select_from_logits(const df2_dims *dims, const float 
  *   W_vocab, W_sel, pred_cb, succ_cb   device memory, as for dflash2_select
  *   lattice_host   float [B*T, k + k*k] host memory, or NULL to skip its copy
  *   draft_ids_host int32 [B*T] host memory
+ *   status_host    optional uint32 in page-locked host memory that receives the device
+ *                  status word (NULL: a pageable word on the stack, which costs a staged
+ *                  copy of about 1.5 us per call on GB300)
  * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) so that the
  * copies run asynchronously; pageable memory works but serialises the host on each copy.
  * The workspace must hold dflash2_select_host_workspace_bytes(dims): the
@@ -156,7 +159,7 @@ DF2_API size_t dflash2_select_host_workspace_bytes(const df2_dims *dims);
 DF2_API df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, const void *W_vocab,
                                        const void *W_sel, const void *pred_cb, const void *succ_cb,
                                        const int32_t *anchor_host, float *lattice_host, int32_t *draft_ids_host,
-                                       void *workspace, size_t workspace_bytes, void *stream);
+                                       uint32_t *status_host, void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---- single steps of the path (same kernels as above), for stage-by-stage checks ---- */
 

@@ -252,8 +252,8 @@ size_t dflash2_select_host_workspace_bytes(const df2_dims *dims)
 
 df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, const void *W_vocab, const void *W_sel,
                                const void *pred_cb, const void *succ_cb, const int32_t *anchor_host,
-                               float *lattice_host, int32_t *draft_ids_host, void *workspace, size_t workspace_bytes,
-                               void *stream)
+                               float *lattice_host, int32_t *draft_ids_host, uint32_t *status_host, void *workspace,
+                               size_t workspace_bytes, void *stream)
 {
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
@@ -287,12 +287,14 @@ df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, co
          cudaMemcpyAsync(lattice_host, s.lattice, R * width * sizeof(float), cudaMemcpyDeviceToHost, st) !=
              cudaSuccess))
         return fail(DF2_ERR_CUDA);
-    // The status word comes back behind the results; a stack destination is pageable
-    // memory, for which the copy returns only once it is complete.
+    // The status word comes back behind the results, into the caller's page-locked word or a
+    // stack word (pageable memory, for which the copy returns only once it is complete).
     uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    uint32_t *dst = status_host ? status_host : &word;
+    if (cudaMemcpyAsync(dst, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
         return fail(DF2_ERR_CUDA);
     DF2_CUDA(cudaStreamSynchronize(st));
+    word = *static_cast<volatile uint32_t *>(dst);
     return word == 0 ? DF2_OK : DF2_ERR_TIMEOUT;
 }
 

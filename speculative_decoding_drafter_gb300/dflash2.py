@@ -86,7 +86,7 @@ def library(path: str | None = None):
                 "dflash2_topk_noalloc": (I, [D, P, P, P, P]),
                 "dflash2_walk_sample": (I, [D, P, ctypes.c_float, ctypes.c_float, P, P, P, P, P]),
                 "dflash2_dynamic_conv": (I, [ctypes.POINTER(ConvDims), P, P, P, P, P, ctypes.c_float, P, P]),
-                "dflash2_select_host": (I, [D, P, P, P, P, P, P, P, P, P, S, P]),
+                "dflash2_select_host": (I, [D, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "dflash2_select_host_workspace_bytes": (S, [D]),
                 "dflash2_selftest_wait_timeout": (I, [ctypes.c_uint32, P, S, P]),
             }
@@ -243,7 +243,7 @@ def dflash2_select(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: 
 
 
 def _select_host_args(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k, T, lattice_host,
-                      draft_ids_host, workspace, stream):
+                      draft_ids_host, workspace, stream, status_host=None):
     """Checks the arguments of dflash2_select_host once; returns (args tuple, tensors kept alive)."""
     d = _dims_of(hidden_host, W_vocab, W_sel, pred_cb, k, T)
     R = d.B * d.T
@@ -263,9 +263,9 @@ def _select_host_args(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host
             _ptr(pred_cb, bf, (d.V, d.D), "pred_cb"), _ptr(succ_cb, bf, (d.V, d.D), "succ_cb"),
             _host_ptr(anchor_host, torch.int32, (d.B,), "anchor_host"),
             _host_ptr(lattice_host, torch.float32, (R, k + k * k), "lattice_host"),
-            _host_ptr(draft_ids_host, torch.int32, (d.B, T), "draft_ids_host"), workspace.ptr, workspace.nbytes,
-            _stream(stream))
-    keep = (d, hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, workspace)
+            _host_ptr(draft_ids_host, torch.int32, (d.B, T), "draft_ids_host"),
+            _host_ptr(status_host, torch.int32, (1,), "status_host"), workspace.ptr, workspace.nbytes, _stream(stream))
+    keep = (d, hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, workspace, status_host)
     return args, keep, lattice_host, draft_ids_host
 
 
@@ -292,10 +292,13 @@ class SelectHostPlan:
     them in place.  Calling returns (lattice_host or None, draft_ids_host)."""
 
     def __init__(self, hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k: int, T: int, *,
-                 lattice_host=None, draft_ids_host=None, workspace: HostWorkspace | None = None, stream=None):
+                 lattice_host=None, draft_ids_host=None, workspace: HostWorkspace | None = None, stream=None,
+                 pinned_status: bool = True):
+        # a page-locked word for the device status (a pageable one costs a staged copy per call)
+        self.status_host = torch.zeros(1, dtype=torch.int32).pin_memory() if pinned_status else None
         self._args, self._keep, self.lattice_host, self.draft_ids_host = _select_host_args(
             hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k, T, lattice_host, draft_ids_host,
-            workspace, stream)
+            workspace, stream, self.status_host)
         self._fn = library().dflash2_select_host
 
     def __call__(self):

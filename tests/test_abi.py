@@ -135,8 +135,8 @@ def test_select_host_workspace_and_rejections(lib):
     h, w, a, lat, dr = 0x300000, 0x200000, 0x310000, 0x320000, 0x330000
 
     def call(dd=d, hidden=h, anchor=a, draft=dr, ws=0x100000, ws_bytes=n, W_vocab=w):
-        return lib.dflash2_select_host(ctypes.byref(dd), hidden, W_vocab, w, w, w, anchor, lat, draft, ws, ws_bytes,
-                                       None)
+        return lib.dflash2_select_host(ctypes.byref(dd), hidden, W_vocab, w, w, w, anchor, lat, draft, None, ws,
+                                       ws_bytes, None)
 
     assert call(hidden=None) == DF2_ERR_INVALID_ARG
     assert call(anchor=None) == DF2_ERR_INVALID_ARG
@@ -146,7 +146,7 @@ def test_select_host_workspace_and_rejections(lib):
     assert call(ws_bytes=base) == DF2_ERR_WORKSPACE  # room for dflash2_select only, not the staging
     assert call(ws=0x100010) == DF2_ERR_WORKSPACE
     # device pointers are checked before any copy is enqueued (W_sel not 16-byte aligned)
-    assert lib.dflash2_select_host(ctypes.byref(d), h, w, w + 8, w, w, a, lat, dr, 0x100000, n, None) == \
+    assert lib.dflash2_select_host(ctypes.byref(d), h, w, w + 8, w, w, a, lat, dr, None, 0x100000, n, None) == \
         DF2_ERR_INVALID_ARG
 
 
