@@ -267,7 +267,8 @@ DF2_API df2_status dflash2_profile_events(void *begin, void *end);
 /* Static description of a status code. */
 DF2_API const char *dflash2_status_string(df2_status status);
 
-/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH (0.2.0: the host-buffer select with
+ * an optional page-locked status word, the bounded-wait self-test). */
 DF2_API int32_t dflash2_version(void);
 
 #ifdef __cplusplus

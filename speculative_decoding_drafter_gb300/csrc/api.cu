@@ -492,6 +492,6 @@ const char *dflash2_status_string(df2_status status)
     }
 }
 
-int32_t dflash2_version(void) { return 100; }
+int32_t dflash2_version(void) { return 200; }
 
 }  // extern "C"

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_version_and_status_strings(lib):
     from speculative_decoding_drafter_gb300 import dflash2
 
-    assert dflash2.dflash2_version() == 100
+    assert dflash2.dflash2_version() == 200
     for s in range(6):
         assert len(dflash2.dflash2_status_string(s)) >= 2
     assert dflash2.dflash2_status_string(99) == "unknown status"
