@@ -148,6 +148,26 @@ def test_select_properties_on_every_row(case):
         assert np.array_equal(draft[:, t], ids.reshape(cfg.B, T, k)[np.arange(cfg.B), t, j]), f"position {t}"
 
 
+def test_select_on_side_streams_matches(case):
+    """The path depends only on the stream it is given: a side stream, and two calls with their own
+    workspaces running concurrently on two streams, give the default-stream bits."""
+    cfg, d = case["cfg"], case["d"]
+    dims = df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, cfg.k, cfg.D)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    torch.cuda.synchronize()
+    for st in streams:
+        with torch.cuda.stream(st):
+            ws = df.Workspace(dims)
+            outs.append(df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"],
+                                          d["anchor"], cfg.k, cfg.T, workspace=ws) + (ws,))
+    torch.cuda.synchronize()
+    for lat, draft, ws in outs:
+        df.dflash2_check_device_status(ws)
+        assert np.array_equal(host(lat).view(np.uint32), case["lat"].view(np.uint32))
+        assert np.array_equal(host(draft), case["draft"])
+
+
 def test_select_host_matches_the_device_path(case):
     """Host buffers in and out: the same kernels on staged copies, so the same bits."""
     cfg, x, d = case["cfg"], case["x"], case["d"]
