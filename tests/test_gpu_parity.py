@@ -168,6 +168,33 @@ def test_select_on_side_streams_matches(case):
         assert np.array_equal(host(draft), case["draft"])
 
 
+def test_select_replays_from_a_cuda_graph(case):
+    """No allocation, no host synchronisation inside: the two launches capture into a CUDA graph
+    (with their programmatic dependency) and every replay gives the direct call's bits."""
+    cfg, d = case["cfg"], case["d"]
+    dims = df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, cfg.k, cfg.D)
+    lat = torch.empty((cfg.R, cfg.k + cfg.k * cfg.k), dtype=torch.float32, device="cuda")
+    draft = torch.empty((cfg.B, cfg.T), dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        ws = df.Workspace(dims)
+        df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], d["anchor"], cfg.k,
+                          cfg.T, lattice=lat, draft_ids=draft, workspace=ws)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], d["anchor"], cfg.k,
+                          cfg.T, lattice=lat, draft_ids=draft, workspace=ws)
+    for _ in range(3):
+        lat.zero_()
+        draft.fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        df.dflash2_check_device_status(ws)
+        assert np.array_equal(host(lat).view(np.uint32), case["lat"].view(np.uint32))
+        assert np.array_equal(host(draft), case["draft"])
+
+
 def test_select_host_matches_the_device_path(case):
     """Host buffers in and out: the same kernels on staged copies, so the same bits."""
     cfg, x, d = case["cfg"], case["x"], case["d"]
