@@ -79,6 +79,8 @@ df2_status check_dims(const df2_dims *d)
 struct Workspace {
     uint32_t *status;
     unsigned *counters;
+    unsigned *group_done;  // LM head: CTAs finished per row group
+    uint32_t *bound;       // LM head: [R, KP] shared lower-bound keys
     float *pval;
     int32_t *pid;
     int32_t *best;
@@ -86,11 +88,18 @@ struct Workspace {
     size_t bytes;
 };
 
-// Control block (zeroed by dflash2_workspace_init): status word, per-sequence counters.
-size_t control_bytes(const df2_dims &d) { return kAlign + round_up(sizeof(unsigned) * static_cast<size_t>(d.B)); }
+// Control block (zeroed by dflash2_workspace_init, left zeroed by every call): status word,
+// per-sequence counters, the LM head's per-row-group counters and per-row bound keys.
+size_t control_bytes(const df2_dims &d)
+{
+    const size_t R = static_cast<size_t>(d.B) * d.T;
+    return kAlign + round_up(sizeof(unsigned) * static_cast<size_t>(d.B)) +
+           round_up(sizeof(unsigned) * static_cast<size_t>(lm_head_max_groups(static_cast<long long>(R)))) +
+           round_up(sizeof(uint32_t) * R * static_cast<size_t>(kp_for(d.k)));
+}
 
-// Layout (each part 256-byte aligned): status word | sequence counters | partial values |
-// partial ids | walk choices | gate.
+// Layout (each part 256-byte aligned): status word | sequence counters | row-group counters |
+// bound keys | partial values | partial ids | walk choices | gate.
 Workspace carve(const df2_dims &d, void *base)
 {
     const size_t R = static_cast<size_t>(d.B) * d.T;
@@ -102,6 +111,10 @@ Workspace carve(const df2_dims &d, void *base)
     off += kAlign;
     w.counters = reinterpret_cast<unsigned *>(p ? p + off : nullptr);
     off += round_up(sizeof(unsigned) * static_cast<size_t>(d.B));
+    w.group_done = reinterpret_cast<unsigned *>(p ? p + off : nullptr);
+    off += round_up(sizeof(unsigned) * static_cast<size_t>(lm_head_max_groups(static_cast<long long>(R))));
+    w.bound = reinterpret_cast<uint32_t *>(p ? p + off : nullptr);
+    off += round_up(sizeof(uint32_t) * R * kp);
     w.pval = reinterpret_cast<float *>(p ? p + off : nullptr);
     const size_t splits = static_cast<size_t>(max_splits_for(static_cast<long long>(R)));
     off += round_up(R * splits * kp * sizeof(float));
@@ -237,8 +250,8 @@ df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *
     float *g = gate ? gate : w.gate;
     int n_split = 0;
     DF2_CUDA(profile_mark(t_profile_begin, st));
-    DF2_CUDA(launch_lm_head(hidden, R, d.H, W_vocab, d.V, kp, w.pval, w.pid, &n_split, W_sel, d.D, g, d.D, w.status,
-                            st));
+    DF2_CUDA(launch_lm_head(hidden, R, d.H, W_vocab, d.V, kp, w.pval, w.pid, &n_split, W_sel, d.D, g, d.D, w.bound,
+                            w.group_done, w.status, st));
     DF2_CUDA(profile_mark(t_profile_end, st));
     return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st);
 }

@@ -9,24 +9,38 @@
 //                  hidden state, stored as float32.
 // Either segment may be empty (the stage entry points use the store segment alone).
 //
-// Design (one CTA per SM, 192 threads, warp-specialised):
+// Design (one CTA per SM, 64 + 128 * mt threads, warp-specialised; mt = row tiles per CTA):
 //   warp 0      TMA producer: per stage, kbs consecutive K-blocks of 64 elements (128
-//               bytes, 128-byte swizzle) of an A box of the live rows (<= 128) and of a
-//               chunk of bn (128 or 256) rows of B.  Up to 64 rows: bn = 128, kbs = 2
-//               (each W row read in 256-byte runs); beyond: bn = 256, kbs = 1.  4-6 stages.
-//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N<=bn,
-//               K=16 per instruction) into one of two bn-column accumulators.
-//   warps 2-5   epilogue: tcgen05.ld the accumulator (thread = one row of C), then keep
-//               a per-row top-KP list in registers (full logits never reach global
-//               memory) or store float32.
-// Work split: CTA (m, s) owns row tile m and a contiguous slice of the columns of both
-// segments (multiples of 16), walked in chunks of <= 256 that never straddle the segment
-// boundary.  CTAs sharing a slice are launched next to each other, so W_vocab is read
-// from HBM about once and re-read from L2 by the other row tiles.
+//               bytes, 128-byte swizzle) of mt A boxes of the live rows (<= 128 each) and
+//               of a chunk of bn (128 or 256) rows of B.  Up to 64 rows: bn = 128, kbs = 2
+//               (each W row read in 256-byte runs); beyond: bn = 256, kbs = 1.
+//   warp 1      allocates 512 TMEM columns and issues tcgen05.mma (M=128, N<=bn, K=16 per
+//               instruction), one per row tile, into bn-column accumulators: two buffers
+//               per tile when they fit (mt = 1), one when two tiles fill TMEM (mt = 2).
+//   warps 2..   epilogue, four warps per row tile: tcgen05.ld the accumulator (thread =
+//               one row of C), then keep a per-row top-KP list in registers (full logits
+//               never reach global memory) or store float32.
+// Two row tiles per CTA (beyond 128 rows) halve what an SM takes in per MMA flop: 64 KB of
+// A and B per 2 x 128x256x64 block instead of 48 KB per 128x256x64, which is what limits
+// the tensor pipe when all SMs stream.
+// Work split: CTA (g, s) owns row group g (mt consecutive row tiles) and a contiguous
+// slice of the columns of both segments (multiples of 16), walked in chunks of <= 256
+// that never straddle the segment boundary.  CTAs sharing a slice are launched next to
+// each other, so W_vocab is read from HBM about once and re-read from L2 by the other
+// row groups.
+// Shared bound (two-tile mode, where the MMA waits for the epilogue): each row has KP
+// slots; after each chunk CTA s raises slot s mod KP to the best logit its slice has
+// given so far (atomicMax on an order-preserving key).  The KP slots then hold logits of
+// KP distinct columns, so their minimum is a lower bound on the row's KP-th best logit,
+// and every CTA's epilogue skips values below it.  A value below the bound is outranked
+// by at least KP others and cannot reach the row's top-k; every value of the top-k still
+// reaches its slice's list, so the merged top-k is exactly the same.  The last CTA of each
+// row group returns its rows' slots to zero.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cfloat>
 #include <cstdint>
 
 #include "internal.h"
@@ -42,13 +56,13 @@ constexpr int BK = 64;                         // K elements per K-block: one 12
 constexpr int UNIT = 16;                       // column granularity of slices and of MMA N
 constexpr int MAX_STAGES = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;      // what one MMA reads of A: 16 KB
-constexpr int THREADS = 192;
+constexpr int MAX_MT = 2;                      // row tiles per CTA
+constexpr int MAX_THREADS = 64 + MAX_MT * BM;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int STASH_STRIDE = 33;               // floats per epilogue thread (32 + 1 pad)
 constexpr int BAR_BYTES = 256;
-constexpr int STASH_BYTES = BM * STASH_STRIDE * 4;
+constexpr int STASH_TILE_BYTES = BM * STASH_STRIDE * 4;
 constexpr int SMEM_LIMIT = 227 * 1024;
-constexpr int STAGE_BUDGET = SMEM_LIMIT - 1024 - BAR_BYTES - STASH_BYTES;
 
 struct GemmArgs {
     int R, K;
@@ -56,6 +70,9 @@ struct GemmArgs {
     int n_topk_pad;   // rounded up to UNIT: start of the store segment in the column space
     int n_store;      // columns of the store segment
     int row_tiles, n_split;
+    int mt;           // row tiles per CTA (1 or 2)
+    int row_groups;   // ceil(row_tiles / mt)
+    int n_bufs;       // accumulator buffers per row tile (2, or 1 when mt tiles fill TMEM)
     int stages;       // pipeline depth
     int bn;           // columns per chunk (128 or 256)
     int kbs;          // K-blocks per stage
@@ -64,8 +81,40 @@ struct GemmArgs {
     int32_t *pid;
     float *out;       // store segment: out[r * ldo + n]
     long long ldo;
+    uint32_t *bound;        // [R, KP] slot keys of the shared bound (null: each CTA alone)
+    unsigned *group_done;   // [row_groups] CTAs finished per row group
     uint32_t *status;
 };
+
+// Order-preserving map of a float to an unsigned key (larger float, larger key); every key
+// of a float is above 0, which marks an empty slot.
+__device__ __forceinline__ uint32_t order_key(float x)
+{
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// The shared bound of one row as a filter threshold: below the minimum slot by at least
+// one float32 step (values equal to the bound must still pass), or -inf while a slot is empty.
+template <int KP>
+__device__ __forceinline__ float shared_threshold(const uint32_t *slots)
+{
+    uint32_t m = 0xffffffffu;
+#pragma unroll
+    for (int q = 0; q < KP / 4; ++q) {
+        const uint4 k4 = __ldcg(reinterpret_cast<const uint4 *>(slots) + q);
+        m = min(m, min(min(k4.x, k4.y), min(k4.z, k4.w)));
+    }
+    if (m == 0u)
+        return -INFINITY;
+    const float t = key_value(m);
+    return t - (fabsf(t) * 0x1p-22f + FLT_MIN);
+}
 
 // One chunk of a CTA's column slice.
 struct Chunk {
@@ -127,7 +176,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 }
 
 template <int KP>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(MAX_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_t_wide,
                    const __grid_constant__ CUtensorMap map_t_narrow, const __grid_constant__ CUtensorMap map_s_wide,
                    const __grid_constant__ CUtensorMap map_s_narrow, const GemmArgs args)
@@ -136,9 +185,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = args.stages;
     const int kbs = args.kbs;
+    const int mt = args.mt;
+    const int n_bufs = args.n_bufs;
     const int b_sub = args.bn * BK * 2;  // bytes of one B K-block of a full chunk
-    // stage layout: kbs A K-blocks, then kbs B K-blocks (every part 1024-byte aligned)
-    const int stage_bytes = kbs * (args.a_bytes + b_sub);
+    // stage layout: kbs x mt A K-blocks (K-block major), then kbs B K-blocks (every part
+    // 1024-byte aligned)
+    const int stage_bytes = kbs * (mt * args.a_bytes + b_sub);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + stages * stage_bytes);
     // bars: full[MAX_STAGES] | empty[MAX_STAGES] | tfull[2] | tempty[2] | drain
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * MAX_STAGES + 5);
@@ -147,8 +199,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m_tile = blockIdx.x % args.row_tiles;
-    const int split = blockIdx.x / args.row_tiles;
+    const int group = blockIdx.x % args.row_groups;
+    const int tile0 = group * mt;
+    const int split = blockIdx.x / args.row_groups;
+    const int tiles = min(mt, args.row_tiles - tile0);  // row tiles this CTA computes
     const Slice slice = slice_of(args, split);
     const int n_chunks = slice.n0 + slice.n1;
     const int kstages = (args.K + BK * kbs - 1) / (BK * kbs);  // stages per chunk
@@ -168,7 +222,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), 4 * 32);
+            mbar_init(tempty_bar(b), tiles * BM);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -204,7 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const Chunk ch = chunk_of(args, slice, c);
                 const CUtensorMap *wide = ch.store ? &map_s_wide : &map_t_wide;
                 const CUtensorMap *narrow = ch.store ? &map_s_narrow : &map_t_narrow;
-                const uint32_t tx = static_cast<uint32_t>(kbs * (args.a_bytes + ch.n * BK * 2));
+                const uint32_t tx = static_cast<uint32_t>(kbs * (tiles * args.a_bytes + ch.n * BK * 2));
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -214,8 +268,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive_expect_tx(full_bar(stage), tx);
                     for (int q = 0; q < kbs; ++q) {
                         const int x = (ks * kbs + q) * BK;  // past K the boxes read zeros
-                        tma_load_2d(smem_u32(st + q * args.a_bytes), &map_a, full_bar(stage), x, m_tile * BM);
-                        const uint32_t b_dst = smem_u32(st + kbs * args.a_bytes + q * b_sub);
+                        for (int t = 0; t < tiles; ++t)
+                            tma_load_2d(smem_u32(st + (q * mt + t) * args.a_bytes), &map_a, full_bar(stage), x,
+                                        (tile0 + t) * BM);
+                        const uint32_t b_dst = smem_u32(st + kbs * mt * args.a_bytes + q * b_sub);
                         // the weights stream through once: evict-first in L2 (measured on GB300:
                         // 197.3 vs 198.0 us at 16 rows, 248.3 vs 250.0 at 64, 449.9 vs 455.1 at 512)
                         if (ch.n == args.bn) {
@@ -247,8 +303,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int c = 0; c < n_chunks && ok; ++c) {
-                const int buf = c & 1;
-                const uint32_t use = static_cast<uint32_t>(c >> 1);
+                const int buf = c % n_bufs;
+                const uint32_t use = static_cast<uint32_t>(c / n_bufs);
                 const Chunk ch = chunk_of(args, slice, c);
                 const uint32_t idesc = idesc_bf16_f32(BM, ch.n);
                 if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag)) {
@@ -256,7 +312,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * args.bn);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * mt * args.bn);
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
@@ -265,12 +321,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const uint32_t st = smem_u32(smem + stage * stage_bytes);
                     for (int q = 0; q < kbs; ++q) {
-                        const uint32_t a0 = st + static_cast<uint32_t>(q * args.a_bytes);
-                        const uint32_t b0 = st + static_cast<uint32_t>(kbs * args.a_bytes + q * b_sub);
+                        const uint32_t b0 = st + static_cast<uint32_t>(kbs * mt * args.a_bytes + q * b_sub);
+                        for (int t = 0; t < tiles; ++t) {
+                            const uint32_t a0 = st + static_cast<uint32_t>((q * mt + t) * args.a_bytes);
+                            const uint32_t d = d_tmem + static_cast<uint32_t>(t * args.bn);
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk)
-                            umma_bf16(d_tmem, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32),
-                                      idesc, (ks | q | kk) != 0 ? 1u : 0u);
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                umma_bf16(d, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
+                                          (ks | q | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     umma_commit(empty_bar(stage));
                     if (++stage == stages) {
@@ -287,18 +346,24 @@ __global__ void __launch_bounds__(THREADS, 1)
                 drain_wait(drain_bar, 0);
             }
         }
-    } else {
-        // ---------------- epilogue: thread = one row of the 128-row tile
+    } else if ((warp - 2) / 4 < tiles) {
+        // ---------------- epilogue: thread = one row of row tile t
+        const int t = (warp - 2) / 4;
         const int q = warp & 3;  // TMEM lane quarter this warp may read
-        const int row = m_tile * BM + q * 32 + lane;
+        const int row = (tile0 + t) * BM + q * 32 + lane;
         const bool row_ok = row < args.R;
-        float *my_stash = stash + (q * 32 + lane) * STASH_STRIDE;
+        float *my_stash = stash + (threadIdx.x - 64) * STASH_STRIDE;
+        const uint32_t acc_col = static_cast<uint32_t>(t * args.bn);
+        uint32_t *slots = args.bound && row_ok ? args.bound + static_cast<long long>(row) * KP : nullptr;
+        float published = -INFINITY;
         ThreadTopK<KP> top;
         top.init();
         for (int c = 0; c < n_chunks; ++c) {
-            const int buf = c & 1;
-            const uint32_t use = static_cast<uint32_t>(c >> 1);
+            const int buf = c % n_bufs;
+            const uint32_t use = static_cast<uint32_t>(c / n_bufs);
             const Chunk ch = chunk_of(args, slice, c);
+            // read before the accumulator is ready: the load's latency hides under the wait
+            const float ext = slots && !ch.store && c > 0 ? shared_threshold<KP>(slots) : -INFINITY;
             const bool ready = mbar_wait(tfull_bar(buf), use & 1u, abort_flag);
             if (!__all_sync(kFullMask, ready))
                 break;
@@ -306,7 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int cb = 0; cb < ch.n / 32 + ((ch.n & 31) ? 1 : 0); ++cb) {
                 uint32_t r[32];
                 tmem_ld_32x32b_x32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                       static_cast<uint32_t>(buf * args.bn + cb * 32),
+                                       static_cast<uint32_t>(buf * mt * args.bn + cb * 32) + acc_col,
                                    r);
                 tmem_wait_ld(r);
                 const int valid = min(32, ch.valid - cb * 32);
@@ -327,13 +392,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 } else if (row_ok && valid > 0) {
-                    const float thr = top.threshold();
-                    uint32_t mask = 0;
+                    const float thr = fmaxf(top.threshold(), ext);
+                    // most blocks hold no value above the threshold: test their maximum first
+                    float m[8];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        mask |= static_cast<uint32_t>(__uint_as_float(r[j]) > thr) << j;
-                    if (valid < 32)
-                        mask &= (1u << valid) - 1u;
+                    for (int j = 0; j < 8; ++j)
+                        m[j] = fmaxf(fmaxf(__uint_as_float(r[j]), __uint_as_float(r[j + 8])),
+                                     fmaxf(__uint_as_float(r[j + 16]), __uint_as_float(r[j + 24])));
+                    const float block_max = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
+                                                  fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+                    uint32_t mask = 0;
+                    if (block_max > thr) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            mask |= static_cast<uint32_t>(__uint_as_float(r[j]) > thr) << j;
+                        if (valid < 32)
+                            mask &= (1u << valid) - 1u;
+                    }
                     if (mask) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
@@ -349,7 +424,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_before();
             mbar_arrive(tempty_bar(buf));
+            if (slots && !ch.store && top.v[0] > published) {
+                atomicMax(slots + split % KP, order_key(top.v[0]));
+                published = top.v[0];
+            }
         }
+        if (slots)
+            __threadfence();  // the slot updates land before this CTA counts itself done
         if (row_ok && args.n_topk > 0) {
             const long long base = (static_cast<long long>(row) * args.n_split + split) * KP;
 #pragma unroll
@@ -369,6 +450,22 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (threadIdx.x == 0 && *abort_flag)
         atomicOr(args.status, kStatusTimeoutGemm);
+    if (args.bound) {
+        // the last CTA of the row group returns the group's slots (and its counter) to zero
+        __shared__ int s_last;
+        if (threadIdx.x == 0)
+            s_last = atomicAdd(args.group_done + group, 1u) == static_cast<unsigned>(args.n_split - 1);
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            const long long k0 = static_cast<long long>(tile0) * BM * KP;
+            const long long k1 = static_cast<long long>(min(args.R, (tile0 + tiles) * BM)) * KP;
+            for (long long i = k0 + threadIdx.x; i < k1; i += blockDim.x)
+                args.bound[i] = 0u;
+            if (threadIdx.x == 0)
+                args.group_done[group] = 0u;
+        }
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
@@ -443,11 +540,18 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     // the tensor cores best (438.5 vs 480.3 us at 512 rows).
     args.bn = R <= 64 ? 128 : BN;
     args.kbs = R <= 64 ? 2 : 1;
-    const int stage_bytes = args.kbs * (args.a_bytes + args.bn * BK * 2);
-    args.stages = std::min(MAX_STAGES, STAGE_BUDGET / stage_bytes);
+    args.row_tiles = (R + BM - 1) / BM;
+    // Beyond 128 rows a CTA takes two row tiles against each chunk of B; their 256-column
+    // accumulators fill TMEM, so the chunk's accumulator is single-buffered.
+    args.mt = args.bn == BN && args.row_tiles >= 2 ? 2 : 1;
+    args.n_bufs = 2 * args.mt * args.bn <= TMEM_COLS ? 2 : 1;
+    args.row_groups = (args.row_tiles + args.mt - 1) / args.mt;
+    const int stash_bytes = args.mt * STASH_TILE_BYTES;
+    const int stage_bytes = args.kbs * (args.mt * args.a_bytes + args.bn * BK * 2);
+    args.stages = std::min(MAX_STAGES, (SMEM_LIMIT - 1024 - BAR_BYTES - stash_bytes) / stage_bytes);
     if (args.stages < 2 || args.a_bytes + args.bn * BK * 2 < A_TILE_BYTES)
         return cudaErrorInvalidConfiguration;
-    const int smem_bytes = 1024 + args.stages * stage_bytes + BAR_BYTES + STASH_BYTES;
+    const int smem_bytes = 1024 + args.stages * stage_bytes + BAR_BYTES + stash_bytes;
 
     CUtensorMap ma, mtw, mtn, msw, msn;
     cudaError_t e;
@@ -472,12 +576,16 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     args.n_topk_pad = (n_topk + UNIT - 1) / UNIT * UNIT;
     args.n_store = n_store;
     const int units = (args.n_topk_pad + n_store + UNIT - 1) / UNIT;
-    args.row_tiles = (R + BM - 1) / BM;
-    args.n_split = std::max(1, std::min({max_splits_for(R), units, std::max(1, sms / args.row_tiles)}));
+    // the shared bound pays where the MMA waits for the epilogue (one accumulator buffer)
+    if (args.n_bufs != 1 || n_topk == 0) {
+        args.bound = nullptr;
+        args.group_done = nullptr;
+    }
+    args.n_split = std::max(1, std::min({max_splits_for(R), units, std::max(1, sms / args.row_groups)}));
     if (n_split_out)
         *n_split_out = args.n_split;
-    const dim3 grid(static_cast<unsigned>(args.row_tiles * args.n_split));
-    gemm_tc_kernel<KP><<<grid, THREADS, smem_bytes, stream>>>(ma, mtw, mtn, msw, msn, args);
+    const dim3 grid(static_cast<unsigned>(args.row_groups * args.n_split));
+    gemm_tc_kernel<KP><<<grid, 64 + args.mt * BM, smem_bytes, stream>>>(ma, mtw, mtn, msw, msn, args);
     return cudaGetLastError();
 }
 
@@ -485,13 +593,16 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
 
 cudaError_t launch_lm_head(const void *hidden, int R, int K, const void *W_vocab, int V, int KP, float *pval,
                            int32_t *pid, int *n_split_out, const void *W_store, int n_store, float *out,
-                           long long ldo, uint32_t *status, cudaStream_t stream)
+                           long long ldo, uint32_t *bound, unsigned *group_done, uint32_t *status,
+                           cudaStream_t stream)
 {
     GemmArgs a{};
     a.pval = pval;
     a.pid = pid;
     a.out = out;
     a.ldo = ldo;
+    a.bound = bound;
+    a.group_done = group_done;
     a.status = status;
     switch (KP) {
     case 4: return launch<4>(hidden, R, K, W_vocab, V, W_store, n_store, a, n_split_out, stream);

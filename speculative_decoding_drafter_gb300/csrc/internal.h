@@ -34,10 +34,16 @@ cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
 // (bf16 in, float32 accumulate).  The first V columns are reduced on the fly to per-row
 // top-KP lists over each CTA's column slice, pval/pid [R, n_split, KP] (value desc, id
 // asc; *n_split_out receives n_split); the next n_store columns (W_store rows) are stored
-// as float32 out[r * ldo + n].  V = 0 or n_store = 0 drops that segment.
+// as float32 out[r * ldo + n].  V = 0 or n_store = 0 drops that segment.  bound [R, KP] and
+// group_done [lm_head_max_groups(R)] are scratch that is zero before the launch and zero
+// again after it: a lower bound on each row's KP-th best logit that the CTAs share.
 cudaError_t launch_lm_head(const void *hidden, int R, int K, const void *W_vocab, int V, int KP, float *pval,
                            int32_t *pid, int *n_split_out, const void *W_store, int n_store, float *out,
-                           long long ldo, uint32_t *status, cudaStream_t stream);
+                           long long ldo, uint32_t *bound, unsigned *group_done, uint32_t *status,
+                           cudaStream_t stream);
+
+// Row groups of the LM head at R rows (at most one per 128-row tile).
+inline int lm_head_max_groups(long long R) { return static_cast<int>((R + 127) / 128); }
 
 // C = A[R, K] . B[N, K]^T stored as float32 out[r * ldo + n] (the store segment alone).
 cudaError_t launch_gemm_store(const void *A, const void *B, int R, int K, int N, float *out, long long ldo,

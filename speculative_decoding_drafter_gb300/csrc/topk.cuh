@@ -39,24 +39,24 @@ struct ThreadTopK {
 
     // Insert when ids arrive in increasing order: an equal value never displaces an
     // entry (the entry has the lower id), so the strict '>' implements the tie-break.
+    // Branch-free: every slot takes its upper neighbour (x ranks above it), x (x lands
+    // here) or itself; slots are visited bottom-up so each reads its neighbour's old value.
     __device__ __forceinline__ void push_increasing_id(float x, int id)
     {
         if (!(x > v[KP - 1]))
             return;
 #pragma unroll
         for (int s = KP - 1; s > 0; --s) {
-            if (x > v[s - 1]) {
-                v[s] = v[s - 1];
-                i[s] = i[s - 1];
-            } else if (x > v[s]) {
-                v[s] = x;
-                i[s] = id;
-            }
+            const bool above = x > v[s - 1];
+            const bool here = x > v[s];
+            const float nv = here ? x : v[s];
+            const int ni = here ? id : i[s];
+            v[s] = above ? v[s - 1] : nv;
+            i[s] = above ? i[s - 1] : ni;
         }
-        if (x > v[0]) {
-            v[0] = x;
-            i[0] = id;
-        }
+        const bool first = x > v[0];
+        v[0] = first ? x : v[0];
+        i[0] = first ? id : i[0];
     }
 
     // Insert under the full order (value desc, id asc), ids in any order.

@@ -329,21 +329,29 @@ def small_case(B, T, H, V, k, D, seed):
 
 
 def run_select(x, cfg):
+    """The whole path.  Also returns the kernel's own float32 unary scores (its top-k logits): the
+    candidate order is checked against these, since two logits that are distinct in the oracle's
+    float64 can round to one float32 value, which the kernel then orders by token id."""
     d = {n: dev_bf16(x[n]) for n in ("hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb")}
+    R = cfg.B * cfg.T
+    ids = torch.empty((R, cfg.k), dtype=torch.int32, device="cuda")
+    vals = torch.empty((R, cfg.k), dtype=torch.float32, device="cuda")
     lat, draft = df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], dev(x["anchor"]),
-                                   cfg.k, cfg.T)
-    return host(lat), host(draft)
+                                   cfg.k, cfg.T, topk_ids=ids, topk_logits=vals)
+    lat = host(lat)
+    assert np.array_equal(host(ids), lat[:, :cfg.k].astype(np.int32))
+    return lat, host(draft), host(vals)
 
 
 @pytest.mark.parametrize("B,T,H,V,k,D", [(1, 1, 64, 16, 1, 8), (3, 7, 200, 1013, 5, 24), (2, 9, 136, 5000, 32, 64),
                                          (9, 16, 512, 3000, 16, 128), (1, 4, 8, 32, 32, 8)])
 def test_select_edge_shapes(B, T, H, V, k, D):
     cfg, x = small_case(B, T, H, V, k, D, seed=B + T + k)
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
     tol = row_tol(ora["logits"])
     ids = lat[:, :k].astype(np.int32)
-    check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+    check_fused_candidates(ids, vals, ora["logits"], ora["topk_ids"],
                            ora["topk_vals"], tol)
     compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
     assert compared + low >= 1
@@ -354,12 +362,12 @@ def test_select_largest_vocabulary():
     B, T, H, V, k, D = 1, 2, 8, (1 << 24) - 1, 32, 8
     cfg, x = small_case(B, T, H, V, k, D, seed=3)
     x["W_vocab"][V - 1] = x["hidden"][0]  # logit |h_0|^2, far above the ~5.6 sigma maximum of the rest
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     assert int(lat[0, 0]) == V - 1 and lat[0, 0] == np.float32(V - 1)
     ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
     tol = row_tol(ora["logits"])
     ids = lat[:, :k].astype(np.int32)
-    check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+    check_fused_candidates(ids, vals, ora["logits"], ora["topk_ids"],
                            ora["topk_vals"], tol)
     compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
     assert compared + low >= 1
@@ -369,7 +377,7 @@ def test_select_most_rows():
     """B*T = 2^20 rows, the row limit: 8192 row tiles in the LM head, 2^20 CTAs in the finish kernel."""
     B, T, H, V, k, D = 65536, 16, 8, 64, 4, 8
     cfg, x = small_case(B, T, H, V, k, D, seed=4)
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     assert lat.shape == (B * T, k + k * k) and draft.shape == (B, T)
     total = 0
     for b in (0, 31337, B - 1):
@@ -378,7 +386,7 @@ def test_select_most_rows():
                             x["anchor"][b:b + 1], k, T)
         tol = row_tol(ora["logits"])
         ids = lat[rows, :k].astype(np.int32)
-        check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+        check_fused_candidates(ids, vals[rows], ora["logits"], ora["topk_ids"],
                                ora["topk_vals"], tol)
         compared, low = compare_lattice_and_draft(lat[rows], draft[b:b + 1], ora, T, k, tol)
         assert compared + low >= 1
@@ -390,11 +398,11 @@ def test_select_long_sequence_walks_from_global_memory():
     """T * k above 8192: the finish kernel's walk reads its choice table from global memory."""
     B, T, H, V, k, D = 2, 300, 64, 5000, 32, 16
     cfg, x = small_case(B, T, H, V, k, D, seed=13)
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
     tol = row_tol(ora["logits"])
     ids = lat[:, :k].astype(np.int32)
-    check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+    check_fused_candidates(ids, vals, ora["logits"], ora["topk_ids"],
                            ora["topk_vals"], tol)
     compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
     assert compared + low >= 1
@@ -408,21 +416,60 @@ def test_select_long_sequence_walks_from_global_memory():
             assert draft[b, t] == int(row[j]), f"sequence {b} position {t}"
 
 
+def _control_bytes(B, T, k):
+    """Bytes of the workspace control block: status word | sequence counters [B] | LM-head
+    row-group counters [ceil(R/128)] | shared-bound slots [R, KP], each part 256-byte aligned."""
+    ru = lambda n: -(-n // 256) * 256
+    R = B * T
+    kp = 4 if k <= 4 else 8 if k <= 8 else 16 if k <= 16 else 32
+    return 256 + ru(4 * B) + ru(4 * -(-R // 128)) + ru(4 * R * kp)
+
+
+@pytest.mark.parametrize("B,T,H,V,k", [(20, 16, 256, 20000, 16), (3, 100, 128, 5000, 32), (1, 16, 256, 4096, 8)])
+def test_select_leaves_control_block_zero(B, T, H, V, k):
+    """Every call returns the workspace's control block to zero, so a call on new inputs after
+    another gives the bits of a fresh workspace (a bound left over from the last call's logits
+    would drop candidates of the next)."""
+    D = 64
+    cfg, xa = small_case(B, T, H, V, k, D, seed=B * T + 1)
+    _, xb = small_case(B, T, H, V, k, D, seed=B * T + 2)
+    xb["hidden"] = (xb["hidden"].astype(np.int32) ^ 0x8000).astype(np.uint16)  # negated: other maxima
+    dims = df.make_dims(B, T, H, V, k, D)
+
+    def run(x, ws):
+        d = {n: dev_bf16(x[n]) for n in ("hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb")}
+        lat, draft = df.dflash2_select(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"],
+                                       dev(x["anchor"]), k, T, workspace=ws)
+        torch.cuda.synchronize()
+        return host(lat), host(draft)
+
+    ws = df.Workspace(dims)
+    n_ctrl = _control_bytes(B, T, k)
+    lat_a, draft_a = run(xa, ws)
+    assert not ws.view[:n_ctrl].any().item(), "control block not zero after a call"
+    lat_b, draft_b = run(xb, ws)
+    assert not ws.view[:n_ctrl].any().item(), "control block not zero after a second call"
+    lat_f, draft_f = run(xb, df.Workspace(dims))
+    assert np.array_equal(lat_b.view(np.uint32), lat_f.view(np.uint32)) and np.array_equal(draft_b, draft_f)
+    lat_a2, draft_a2 = run(xa, ws)
+    assert np.array_equal(lat_a.view(np.uint32), lat_a2.view(np.uint32)) and np.array_equal(draft_a, draft_a2)
+
+
 def test_zeroed_codebooks_give_per_position_top1():
     cfg, x = small_case(4, 6, 256, 2048, 8, 32, seed=5)
     x["pred_cb"][:] = 0
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     assert np.array_equal(draft.reshape(-1), lat[:, 0].astype(np.int32))
     x2 = dict(x)
     x2["succ_cb"] = np.zeros_like(x["succ_cb"])
     x2["pred_cb"] = make_inputs(cfg, 5)["pred_cb"]
-    lat2, draft2 = run_select(x2, cfg)
+    lat2, draft2, _ = run_select(x2, cfg)
     assert np.array_equal(draft2.reshape(-1), lat2[:, 0].astype(np.int32))
 
 
 def test_k1_walk_is_top1():
     cfg, x = small_case(3, 5, 128, 777, 1, 16, seed=9)
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], 1, 5)
     assert lat.shape == (15, 2)
     assert np.array_equal(draft.reshape(-1), lat[:, 0].astype(np.int32))
@@ -559,15 +606,28 @@ def _random_shapes(n, seed):
     return out
 
 
-@pytest.mark.parametrize("B,T,H,V,k,D", _random_shapes(24, 2024))
+def _random_multi_tile_shapes(n, seed):
+    """129 to 700 rows: LM-head CTAs that take two 128-row tiles, odd tile counts (a CTA left
+    with one tile) and ragged last tiles."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        k = int(rng.integers(1, 33))
+        T = int(rng.integers(1, 18))
+        B = int(rng.integers(-(-129 // T), 700 // T + 1))
+        out.append((B, T, 8 * int(rng.integers(1, 33)), int(rng.integers(k, 5001)), k, 8 * int(rng.integers(1, 17))))
+    return out
+
+
+@pytest.mark.parametrize("B,T,H,V,k,D", _random_shapes(24, 2024) + _random_multi_tile_shapes(8, 2025))
 def test_select_random_shapes(B, T, H, V, k, D):
     """Seeded random shapes across the limits: the fused path against the oracle under the same rules."""
     cfg, x = small_case(B, T, H, V, k, D, seed=B * 1000 + T * 10 + k)
-    lat, draft = run_select(x, cfg)
+    lat, draft, vals = run_select(x, cfg)
     ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
     tol = row_tol(ora["logits"])
     ids = lat[:, :k].astype(np.int32)
-    swaps = check_fused_candidates(ids, np.take_along_axis(ora["logits"], ids, 1), ora["logits"], ora["topk_ids"],
+    swaps = check_fused_candidates(ids, vals, ora["logits"], ora["topk_ids"],
                                    ora["topk_vals"], tol)
     assert swaps <= max(1, (B * T) // 20)
     compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
