@@ -358,6 +358,18 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
         float published = -INFINITY;
         ThreadTopK<KP> top;
         top.init();
+        // values waiting for insertion, newest first (column ids increase with age reversed)
+        constexpr int kQueue = 4;
+        float queue_v[kQueue];
+        int queue_i[kQueue];
+        int n_queued = 0;
+        auto drain_queue = [&]() {
+#pragma unroll
+            for (int e = kQueue - 1; e >= 0; --e)
+                if (e < n_queued)
+                    top.push_increasing_id(queue_v[e], queue_i[e]);
+            n_queued = 0;
+        };
         for (int c = 0; c < n_chunks; ++c) {
             const int buf = c % n_bufs;
             const uint32_t use = static_cast<uint32_t>(c / n_bufs);
@@ -401,29 +413,43 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
                                      fmaxf(__uint_as_float(r[j + 16]), __uint_as_float(r[j + 24])));
                     const float block_max = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
                                                   fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-                    uint32_t mask = 0;
                     if (block_max > thr) {
+                        uint32_t mask = 0;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             mask |= static_cast<uint32_t>(__uint_as_float(r[j]) > thr) << j;
                         if (valid < 32)
                             mask &= (1u << valid) - 1u;
-                    }
-                    if (mask) {
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            my_stash[j] = __uint_as_float(r[j]);
                         const int base_col = ch.c0 + cb * 32;
-                        while (mask) {
-                            const int j = __ffs(mask) - 1;
-                            mask &= mask - 1u;
-                            top.push_increasing_id(my_stash[j], base_col + j);
+                        if (valid == 32 && __popc(mask) == 1 && n_queued < kQueue && block_max != 0.0f) {
+                            // a single value passes, so it is the block's maximum: queue it
+                            // and insert it once the accumulator is released (a zero goes the
+                            // exact way below, where its sign is the accumulator's)
+#pragma unroll
+                            for (int e = kQueue - 1; e > 0; --e) {
+                                queue_v[e] = queue_v[e - 1];
+                                queue_i[e] = queue_i[e - 1];
+                            }
+                            queue_v[0] = block_max;
+                            queue_i[0] = base_col + __ffs(mask) - 1;
+                            ++n_queued;
+                        } else if (mask) {
+                            drain_queue();  // ids must reach the list in increasing order
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                my_stash[j] = __uint_as_float(r[j]);
+                            while (mask) {
+                                const int j = __ffs(mask) - 1;
+                                mask &= mask - 1u;
+                                top.push_increasing_id(my_stash[j], base_col + j);
+                            }
                         }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(tempty_bar(buf));
+            drain_queue();  // overlaps the next chunk's MMAs
             if (slots && !ch.store && top.v[0] > published) {
                 atomicMax(slots + split % KP, order_key(top.v[0]));
                 published = top.v[0];
