@@ -56,8 +56,6 @@ constexpr int BK = 64;                         // K elements per K-block: one 12
 constexpr int UNIT = 16;                       // column granularity of slices and of MMA N
 constexpr int MAX_STAGES = 8;
 constexpr int A_TILE_BYTES = BM * BK * 2;      // what one MMA reads of A: 16 KB
-constexpr int MAX_MT = 2;                      // row tiles per CTA
-constexpr int MAX_THREADS = 64 + MAX_MT * BM;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int STASH_STRIDE = 33;               // floats per epilogue thread (32 + 1 pad)
 constexpr int BAR_BYTES = 256;
@@ -175,8 +173,11 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
             return;
 }
 
-template <int KP>
-__global__ void __launch_bounds__(MAX_THREADS, 1)
+// MT (row tiles per CTA) is a template parameter: with one tile the per-tile loops must
+// vanish at compile time (a loop of one run-time iteration around the TMA and MMA issue cost
+// 3% at 16 rows, measured on GB300).
+template <int KP, int MT>
+__global__ void __launch_bounds__(64 + MT * BM, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_t_wide,
                    const __grid_constant__ CUtensorMap map_t_narrow, const __grid_constant__ CUtensorMap map_s_wide,
                    const __grid_constant__ CUtensorMap map_s_narrow, const GemmArgs args)
@@ -185,8 +186,8 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int stages = args.stages;
     const int kbs = args.kbs;
-    const int mt = args.mt;
-    const int n_bufs = args.n_bufs;
+    constexpr int mt = MT;
+    constexpr int n_bufs = 2 * MT * BN <= TMEM_COLS ? 2 : 1;  // bn = 256 whenever MT = 2
     const int b_sub = args.bn * BK * 2;  // bytes of one B K-block of a full chunk
     // stage layout: kbs x mt A K-blocks (K-block major), then kbs B K-blocks (every part
     // 1024-byte aligned)
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(MAX_THREADS, 1)
     const int group = blockIdx.x % args.row_groups;
     const int tile0 = group * mt;
     const int split = blockIdx.x / args.row_groups;
-    const int tiles = min(mt, args.row_tiles - tile0);  // row tiles this CTA computes
+    const int tiles = MT == 1 ? 1 : min(MT, args.row_tiles - tile0);  // row tiles this CTA computes
     const Slice slice = slice_of(args, split);
     const int n_chunks = slice.n0 + slice.n1;
     const int kstages = (args.K + BK * kbs - 1) / (BK * kbs);  // stages per chunk
@@ -592,7 +593,7 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
         (e = make_map(&mtn, tb, K, tn, UNIT)) != cudaSuccess ||
         (e = make_map(&msw, sb, K, sn, args.bn)) != cudaSuccess || (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
         return e;
-    auto kern = gemm_tc_kernel<KP>;
+    auto kern = args.mt == 1 ? gemm_tc_kernel<KP, 1> : gemm_tc_kernel<KP, 2>;
     if ((e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem_bytes)) != cudaSuccess)
         return e;
     const int sms = device_sm_count();
@@ -611,7 +612,7 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     if (n_split_out)
         *n_split_out = args.n_split;
     const dim3 grid(static_cast<unsigned>(args.row_groups * args.n_split));
-    gemm_tc_kernel<KP><<<grid, 64 + args.mt * BM, smem_bytes, stream>>>(ma, mtw, mtn, msw, msn, args);
+    kern<<<grid, 64 + args.mt * BM, smem_bytes, stream>>>(ma, mtw, mtn, msw, msn, args);
     return cudaGetLastError();
 }
 
