@@ -88,9 +88,10 @@ typedef struct df2_dims {
 
 /* Bytes of device workspace the calls below need for `dims` (0 if dims are invalid).
  * Independent of the device.  The workspace starts with a control block (the sticky
- * device status word and one completion counter per sequence) that must be zero before
- * the first call: dflash2_workspace_init zeroes it (a zero-filled allocation also works).
- * Calls leave the counters at zero, so a workspace is reused without re-initialising;
+ * device status word, one completion counter per sequence, and the LM head's per-row-group
+ * counters and per-row bound slots) that must be zero before the first call:
+ * dflash2_workspace_init zeroes it (a zero-filled allocation also works).
+ * Calls leave the control block at zero, so a workspace is reused without re-initialising;
  * after a DF2_ERR_TIMEOUT, initialise it again.  One workspace serves one stream at a time. */
 DF2_API size_t dflash2_workspace_bytes(const df2_dims *dims);
 

@@ -148,7 +148,7 @@ def dflash2_workspace_bytes(dims: Dims) -> int:
 
 
 def dflash2_workspace_init(workspace: "Workspace", stream=None) -> None:
-    """Zero the workspace's control block (status word, per-sequence counters) on the stream."""
+    """Zero the workspace's control block (status word, counters, the LM head's bound slots) on the stream."""
     _check(library().dflash2_workspace_init(ctypes.byref(workspace.dims), workspace.ptr, workspace.nbytes,
                                             _stream(stream)), "dflash2_workspace_init")
 
