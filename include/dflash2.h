@@ -136,22 +136,28 @@ DF2_API df2_status dflash2_select_from_logits(const df2_dims *dims, const float 
 /*
  * dflash2_select for a caller whose step inputs and results live in host memory (the
  * drafting loop of a serving engine that feeds hidden states in and reads the draft out
- * each step).  One call enqueues, on `stream`: the copy of hidden and anchor to device
- * staging inside the workspace, the same two launches as dflash2_select, the copies of
- * draft_ids (and of the lattice, if lattice_host is not NULL) back to host, and a copy of
- * the device status word; it then waits for the stream.  Unlike every other call it
- * returns only when the results are in host memory, and it also reports
- * DF2_ERR_TIMEOUT from the device status word (then re-initialise the workspace).
+ * each step).  One call enqueues, on `stream`: the copy of hidden to device staging
+ * inside the workspace, the same two launches as dflash2_select, and the return of the
+ * results; it then waits for the stream.  When anchor_host, draft_ids_host, lattice_host
+ * (if not NULL) and status_host are all page-locked memory mapped into the current
+ * device's address space (cudaHostAlloc / cudaMallocHost, or cudaHostRegister with
+ * cudaHostRegisterMapped) and 4-byte aligned, the finish kernel reads the anchors from
+ * and writes the draft ids, lattice rows and device status word into them directly, with
+ * no copies (each copy on a stream costs about 3 us on GB300, whatever its size).
+ * Otherwise the anchors are copied in and the results and status word copied back.
+ * Unlike every other call it returns only when the results are in host memory, and it
+ * also reports DF2_ERR_TIMEOUT from the device status word (then re-initialise the
+ * workspace).
  *   hidden_host    bf16 [B*T, H], host memory
  *   anchor_host    int32 [B], host memory
  *   W_vocab, W_sel, pred_cb, succ_cb   device memory, as for dflash2_select
  *   lattice_host   float [B*T, k + k*k] host memory, or NULL to skip its copy
  *   draft_ids_host int32 [B*T] host memory
  *   status_host    optional uint32 in page-locked host memory that receives the device
- *                  status word (NULL: a pageable word on the stack, which costs a staged
- *                  copy of about 1.5 us per call on GB300)
- * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) so that the
- * copies run asynchronously; pageable memory works but serialises the host on each copy.
+ *                  status word (NULL: a pageable word on the stack and the copy path)
+ * Host buffers should be page-locked: hidden_host so that its copy runs asynchronously,
+ * the others for the direct path; pageable memory works but serialises the host on each
+ * copy.
  * The workspace must hold dflash2_select_host_workspace_bytes(dims): the
  * dflash2_workspace_bytes layout followed by the device staging of hidden, anchor,
  * lattice and draft.  Nothing is allocated.

@@ -186,12 +186,51 @@ cudaError_t profile_mark(cudaEvent_t ev, cudaStream_t st) { return ev ? cudaEven
 // Shared tail of both select paths: merge, lattice and walk in one launch.
 df2_status finish(const df2_dims &d, const Workspace &w, int n_split, const float *gate, const void *pred_cb,
                   const void *succ_cb, const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
-                  float *topk_vals, cudaStream_t st)
+                  float *topk_vals, cudaStream_t st, const HostMirrors &mirrors = HostMirrors{})
 {
     DF2_CUDA(launch_finish(d.B, d.T, d.k, d.V, d.D, kp_for(d.k), n_split, w.pval, w.pid, gate,
                            static_cast<const uint16_t *>(pred_cb), static_cast<const uint16_t *>(succ_cb), anchor,
-                           lattice, draft_ids, topk_ids, topk_vals, w.best, w.counters, st));
+                           lattice, draft_ids, topk_ids, topk_vals, w.best, w.counters, mirrors, st));
     return DF2_OK;
+}
+
+// The fused path after argument checks: LM head (top-k, gate) and the finish launch.
+df2_status select_checked(const df2_dims &d, const void *hidden, const void *W_vocab, const void *W_sel,
+                          const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,
+                          int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate, void *workspace,
+                          cudaStream_t st, const HostMirrors &mirrors = HostMirrors{})
+{
+    const Workspace w = carve(d, workspace);
+    const int R = d.B * d.T;
+    const int kp = kp_for(d.k);
+    float *g = gate ? gate : w.gate;
+    int n_split = 0;
+    DF2_CUDA(profile_mark(t_profile_begin, st));
+    DF2_CUDA(launch_lm_head(hidden, R, d.H, W_vocab, d.V, kp, w.pval, w.pid, &n_split, W_sel, d.D, g, d.D, w.bound,
+                            w.group_done, w.status, st));
+    DF2_CUDA(profile_mark(t_profile_end, st));
+    HostMirrors m = mirrors;
+    m.status_dev = w.status;
+    return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st, m);
+}
+
+// Device-visible address of a caller's host buffer if it is page-locked memory mapped into
+// this device's address space (the finish kernel may then write it directly), else null.
+template <typename Ptr>
+Ptr *device_view(Ptr *host)
+{
+    if (!host)
+        return nullptr;
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    int dev = -1;
+    if (attr.type != cudaMemoryTypeHost || !attr.devicePointer || cudaGetDevice(&dev) != cudaSuccess ||
+        attr.device != dev)
+        return nullptr;
+    return static_cast<Ptr *>(attr.devicePointer);
 }
 
 df2_status check_tail_pointers(const void *W_sel, const void *pred_cb, const void *succ_cb, const int32_t *anchor,
@@ -243,17 +282,8 @@ df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *
     DF2_TRY(check_tail_pointers(W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, gate));
     DF2_TRY(check_workspace(d, workspace, workspace_bytes));
     cudaGetLastError();  // clear a stale error so the status reflects this call
-    const Workspace w = carve(d, workspace);
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int R = d.B * d.T;
-    const int kp = kp_for(d.k);
-    float *g = gate ? gate : w.gate;
-    int n_split = 0;
-    DF2_CUDA(profile_mark(t_profile_begin, st));
-    DF2_CUDA(launch_lm_head(hidden, R, d.H, W_vocab, d.V, kp, w.pval, w.pid, &n_split, W_sel, d.D, g, d.D, w.bound,
-                            w.group_done, w.status, st));
-    DF2_CUDA(profile_mark(t_profile_end, st));
-    return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st);
+    return select_checked(d, hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids,
+                          topk_logits, gate, workspace, static_cast<cudaStream_t>(stream));
 }
 
 size_t dflash2_select_host_workspace_bytes(const df2_dims *dims)
@@ -288,24 +318,44 @@ df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, co
         return e;
     };
     if (cudaMemcpyAsync(s.hidden, hidden_host, R * d.H * sizeof(uint16_t), cudaMemcpyHostToDevice, st) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(s.anchor, anchor_host, d.B * sizeof(int32_t), cudaMemcpyHostToDevice, st) != cudaSuccess)
+        cudaSuccess)
         return fail(DF2_ERR_CUDA);
-    const df2_status e = dflash2_select(dims, s.hidden, W_vocab, W_sel, pred_cb, succ_cb, s.anchor, s.lattice,
-                                        s.draft, nullptr, nullptr, nullptr, workspace, workspace_bytes, stream);
+    // Page-locked host buffers mapped into this device's address space are read and written
+    // by the finish kernel itself: every copy on the stream costs about 3 us whatever its size
+    // (measured on GB300), and this takes four of the five off the step.  Other buffers go
+    // through copies.  The lookups run while the hidden states upload.
+    const int32_t *anchor_dv = device_view(anchor_host);
+    int32_t *draft_dv = device_view(draft_ids_host);
+    float *lattice_dv = device_view(lattice_host);
+    uint32_t *status_dv = device_view(status_host);
+    const bool direct = anchor_dv && draft_dv && status_dv && (!lattice_host || lattice_dv) && aligned(anchor_dv, 4) &&
+                        aligned(draft_dv, 4) && aligned(status_dv, 4) && (!lattice_dv || aligned(lattice_dv, 4));
+    HostMirrors mirrors;
+    if (direct) {
+        mirrors.lattice = lattice_dv;
+        mirrors.draft = draft_dv;
+        mirrors.status = status_dv;
+    } else if (cudaMemcpyAsync(s.anchor, anchor_host, d.B * sizeof(int32_t), cudaMemcpyHostToDevice, st) !=
+               cudaSuccess) {
+        return fail(DF2_ERR_CUDA);
+    }
+    const df2_status e = select_checked(d, s.hidden, W_vocab, W_sel, pred_cb, succ_cb, direct ? anchor_dv : s.anchor,
+                                        s.lattice, s.draft, nullptr, nullptr, nullptr, workspace, st, mirrors);
     if (e != DF2_OK)
         return fail(e);
-    if (cudaMemcpyAsync(draft_ids_host, s.draft, R * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
-        (lattice_host &&
-         cudaMemcpyAsync(lattice_host, s.lattice, R * width * sizeof(float), cudaMemcpyDeviceToHost, st) !=
-             cudaSuccess))
-        return fail(DF2_ERR_CUDA);
-    // The status word comes back behind the results, into the caller's page-locked word or a
-    // stack word (pageable memory, for which the copy returns only once it is complete).
     uint32_t word = 0;
     uint32_t *dst = status_host ? status_host : &word;
-    if (cudaMemcpyAsync(dst, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
-        return fail(DF2_ERR_CUDA);
+    if (!direct) {
+        if (cudaMemcpyAsync(draft_ids_host, s.draft, R * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+            (lattice_host &&
+             cudaMemcpyAsync(lattice_host, s.lattice, R * width * sizeof(float), cudaMemcpyDeviceToHost, st) !=
+                 cudaSuccess))
+            return fail(DF2_ERR_CUDA);
+        // The status word comes back behind the results, into the caller's page-locked word or a
+        // stack word (pageable memory, for which the copy returns only once it is complete).
+        if (cudaMemcpyAsync(dst, workspace, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return fail(DF2_ERR_CUDA);
+    }
     DF2_CUDA(cudaStreamSynchronize(st));
     word = *static_cast<volatile uint32_t *>(dst);
     return word == 0 ? DF2_OK : DF2_ERR_TIMEOUT;

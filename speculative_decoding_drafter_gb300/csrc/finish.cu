@@ -13,7 +13,11 @@
 //      T choice rows and candidate ids into shared memory and follows j_t = best[t][j_(t-1)].
 //      The counter returns to zero.
 // Launched with programmatic stream serialisation: its prologue overlaps the tail of the
-// kernel that produced the lists, and griddep_wait() orders the reads after it.
+// kernel that produced the lists, and griddep_wait() orders the reads after it (the anchor,
+// which no earlier kernel of the call writes, is read before).
+// Host mirrors (the host-buffer call with page-locked buffers): the lattice rows and draft
+// ids are written to the caller's host buffers as well, and the device status word, final
+// once the LM head is done, to the caller's host status word; no copies follow the kernel.
 #include <cstdint>
 
 #include "internal.h"
@@ -39,6 +43,10 @@ struct FinishArgs {
     int32_t *best;       // [B*T, k] walk choices
     unsigned *counters;  // [B], zero between calls
     int walk_in_smem;    // the sequence's choice table fits the dynamic shared memory
+    float *lattice_mirror;          // optional host mirrors (may be null)
+    int32_t *draft_mirror;
+    const uint32_t *status;         // device status word, copied to status_mirror if set
+    uint32_t *status_mirror;
 };
 
 constexpr int kFinishThreads = 128;
@@ -52,11 +60,15 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
     __shared__ float s_unary[32];
     __shared__ int s_last;
 
-    griddep_wait();
-
     const int r = blockIdx.x;
     const int b = r / a.T;
     const int t = r - b * a.T;
+    const int anchor_b = t == 0 && threadIdx.x == 0 ? a.anchor[b] : 0;
+
+    griddep_wait();
+    if (a.status_mirror && r == 0 && threadIdx.x == 0)
+        *a.status_mirror = *reinterpret_cast<const volatile uint32_t *>(a.status);
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int k = a.k;
@@ -120,7 +132,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
                       blockDim.x - 64);
     }
     if (t == 0 && threadIdx.x == 0)
-        s_prev[0] = clamp_id(a.anchor[b], a.V);
+        s_prev[0] = clamp_id(anchor_b, a.V);
     __syncthreads();
     if (threadIdx.x < k) {
         const long long o = static_cast<long long>(r) * k + threadIdx.x;
@@ -133,7 +145,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
     // ---- 2. lattice row and the walk's choice from each predecessor row
     const long long width = k + static_cast<long long>(k) * k;
     lattice_row<KP>(k, a.D, t == 0 ? 1 : k, s_prev, s_cand, s_unary, a.pred_cb, a.succ_cb, smem,
-                    a.lattice + r * width, a.best + static_cast<long long>(r) * k);
+                    a.lattice + r * width, a.best + static_cast<long long>(r) * k,
+                    a.lattice_mirror ? a.lattice_mirror + r * width : nullptr);
 
     // ---- 3. the last CTA of the sequence walks it
     __threadfence();
@@ -148,6 +161,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
     const int32_t *best = a.best + r0 * k;
     const float *rows = a.lattice + r0 * width;
     int32_t *draft = a.draft + r0;
+    int32_t *draft_mirror = a.draft_mirror ? a.draft_mirror + r0 : nullptr;
     if (a.walk_in_smem) {
         int *sb = reinterpret_cast<int *>(smem);     // [T][k] choices
         int *sid = sb + a.T * k;                     // [T][k] candidate ids
@@ -162,13 +176,18 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
             for (int tt = 0; tt < a.T; ++tt) {
                 j = sb[tt * k + j];
                 draft[tt] = sid[tt * k + j];
+                if (draft_mirror)
+                    draft_mirror[tt] = sid[tt * k + j];
             }
         }
     } else if (threadIdx.x == 0) {
         int j = 0;
         for (int tt = 0; tt < a.T; ++tt) {
             j = __ldcg(best + static_cast<long long>(tt) * k + j);
-            draft[tt] = static_cast<int32_t>(__ldcg(rows + tt * width + j));
+            const int32_t id = static_cast<int32_t>(__ldcg(rows + tt * width + j));
+            draft[tt] = id;
+            if (draft_mirror)
+                draft_mirror[tt] = id;
         }
     }
     if (threadIdx.x == 0)
@@ -209,9 +228,14 @@ cudaError_t launch_kp(FinishArgs a, int B, cudaStream_t stream)
 cudaError_t launch_finish(int B, int T, int k, int V, int D, int KP, int n_split, const float *pval,
                           const int32_t *pid, const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
                           const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
-                          float *topk_vals, int32_t *best, unsigned *counters, cudaStream_t stream)
+                          float *topk_vals, int32_t *best, unsigned *counters, const HostMirrors &mirrors,
+                          cudaStream_t stream)
 {
     FinishArgs a{};
+    a.lattice_mirror = mirrors.lattice;
+    a.draft_mirror = mirrors.draft;
+    a.status = mirrors.status_dev;
+    a.status_mirror = mirrors.status;
     a.T = T;
     a.k = k;
     a.V = V;

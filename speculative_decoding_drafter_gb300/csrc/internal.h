@@ -57,14 +57,25 @@ cudaError_t launch_logits_topk_partial(const float *logits, int R, int V, int KP
 cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int n_split, int KP, int k,
                               int32_t *topk_ids, float *topk_vals, cudaStream_t stream);
 
+// Device-visible pointers into a caller's page-locked host buffers, written by the finish
+// kernel in place of copies after it (each may be null).
+struct HostMirrors {
+    float *lattice = nullptr;            // [B*T, k + k*k]
+    int32_t *draft = nullptr;            // [B*T]
+    uint32_t *status = nullptr;          // one word: receives *status_dev
+    const uint32_t *status_dev = nullptr;
+};
+
 // Everything after the lists in one launch (programmatic dependent launch): merge of
 // the [R, n_split, KP] lists, lattice rows, and the walk by the last CTA of each
 // sequence (best [R, k] is scratch for the walk's choices).  counters [B] must be zero
-// before the call and are zero after it.
+// before the call and are zero after it.  anchor is read before the kernel waits for the
+// one before it, so no kernel of the same call may write it.
 cudaError_t launch_finish(int B, int T, int k, int V, int D, int KP, int n_split, const float *pval,
                           const int32_t *pid, const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
                           const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
-                          float *topk_vals, int32_t *best, unsigned *counters, cudaStream_t stream);
+                          float *topk_vals, int32_t *best, unsigned *counters, const HostMirrors &mirrors,
+                          cudaStream_t stream);
 
 // Packed lattice rows [B*T, k + k*k] from candidates, unary scores, gate and codebooks.
 cudaError_t launch_lattice(int B, int T, int k, int V, int D, const int32_t *topk_ids, const float *topk_vals,

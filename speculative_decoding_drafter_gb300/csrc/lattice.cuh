@@ -69,12 +69,14 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[KP])
 // scores are copied to all k predecessor rows), cand/unary the current candidates, and
 // sg the gate row, already in shared memory at the start of `smem`.
 // If `best` is not null, best[i] receives the walk's choice from predecessor row i:
-// the index of the row's maximum, lowest index on ties.
+// the index of the row's maximum, lowest index on ties.  If `mirror` is not null the row is
+// written there too (a row of a caller's page-locked host buffer).
 // All CTA threads call it; it starts and ends with __syncthreads().
 template <int KP>
 __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const int *s_cand, const float *s_unary,
                             const uint16_t *__restrict__ pred_cb, const uint16_t *__restrict__ succ_cb,
-                            uint8_t *smem, float *__restrict__ out, int32_t *__restrict__ best = nullptr)
+                            uint8_t *smem, float *__restrict__ out, int32_t *__restrict__ best = nullptr,
+                            float *__restrict__ mirror = nullptr)
 {
     constexpr int kBatch = 8;  // 16-byte gathers in flight per thread
     const float *sg = reinterpret_cast<const float *>(smem);                  // [D] gate
@@ -143,10 +145,15 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
             const float s = lane < k ? s_unary[lane] + (h == 0 ? tot0 : tot1) : -INFINITY;
             if (lane < k) {
                 if (n_prev == 1) {
-                    for (int ii = 0; ii < k; ++ii)
+                    for (int ii = 0; ii < k; ++ii) {
                         out[k + ii * k + lane] = s;
+                        if (mirror)
+                            mirror[k + ii * k + lane] = s;
+                    }
                 } else {
                     out[k + i * k + lane] = s;
+                    if (mirror)
+                        mirror[k + i * k + lane] = s;
                 }
             }
             if (best) {
@@ -165,8 +172,11 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
             }
         }
     }
-    if (threadIdx.x < k)
+    if (threadIdx.x < k) {
         out[threadIdx.x] = static_cast<float>(s_cand[threadIdx.x]);
+        if (mirror)
+            mirror[threadIdx.x] = static_cast<float>(s_cand[threadIdx.x]);
+    }
     __syncthreads();
 }
 

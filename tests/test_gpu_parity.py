@@ -223,6 +223,37 @@ def test_select_host_matches_the_device_path(case):
     assert np.array_equal(lat4.numpy()[:, :k], np.tile(np.arange(k, dtype=np.float32), (cfg.R, 1)))  # all-zero logits
 
 
+def test_select_host_paths_agree(case):
+    """Page-locked host buffers are read and written by the finish kernel itself; a pageable
+    buffer among them sends the call through copies.  Both give the device path's bits, and the
+    direct path overwrites whatever the host buffers held."""
+    cfg, x, d = case["cfg"], case["x"], case["d"]
+    h_hidden = torch.from_numpy(x["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    hw = df.HostWorkspace(df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, cfg.k, cfg.D))
+    for anchor_pinned in (True, False):
+        h_anchor = torch.from_numpy(x["anchor"].copy())
+        if anchor_pinned:
+            h_anchor = h_anchor.pin_memory()
+        plan = df.SelectHostPlan(h_hidden, d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], h_anchor, cfg.k,
+                                 cfg.T, workspace=hw)
+        for _ in range(2):
+            plan.lattice_host.fill_(float("nan"))
+            plan.draft_ids_host.fill_(-3)
+            lat, draft = plan()
+            assert np.array_equal(lat.numpy().view(np.uint32), case["lat"].view(np.uint32)), anchor_pinned
+            assert np.array_equal(draft.numpy(), case["draft"]), anchor_pinned
+    # new anchors written in place reach the next call on the direct path
+    h_anchor = torch.from_numpy(x["anchor"].copy()).pin_memory()
+    plan = df.SelectHostPlan(h_hidden, d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], h_anchor, cfg.k, cfg.T,
+                             workspace=hw)
+    plan()
+    h_anchor.copy_(torch.from_numpy((x["anchor"] + 1) % cfg.V))
+    lat_h, _ = plan()
+    dl, dd = df.dflash2_select(dev_bf16(x["hidden"]), d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"],
+                               dev((x["anchor"] + 1) % cfg.V), cfg.k, cfg.T)
+    assert np.array_equal(lat_h.numpy().view(np.uint32), host(dl).view(np.uint32))
+
+
 def test_duplicate_logits_break_ties_by_lower_id(case):
     if case["cfg"].plant != "dup_logits":
         pytest.skip("config has no duplicate logits")
