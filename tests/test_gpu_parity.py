@@ -228,9 +228,11 @@ def test_select_host_paths_agree(case):
     buffer among them sends the call through copies.  Both give the device path's bits, and the
     direct path overwrites whatever the host buffers held."""
     cfg, x, d = case["cfg"], case["x"], case["d"]
-    h_hidden = torch.from_numpy(x["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     hw = df.HostWorkspace(df.make_dims(cfg.B, cfg.T, cfg.H, cfg.V, cfg.k, cfg.D))
-    for anchor_pinned in (True, False):
+    for hidden_pinned, anchor_pinned in ((True, True), (True, False), (False, True)):
+        h_hidden = torch.from_numpy(x["hidden"].copy().view(np.int16)).view(torch.bfloat16)
+        if hidden_pinned:
+            h_hidden = h_hidden.pin_memory()
         h_anchor = torch.from_numpy(x["anchor"].copy())
         if anchor_pinned:
             h_anchor = h_anchor.pin_memory()
@@ -240,9 +242,11 @@ def test_select_host_paths_agree(case):
             plan.lattice_host.fill_(float("nan"))
             plan.draft_ids_host.fill_(-3)
             lat, draft = plan()
-            assert np.array_equal(lat.numpy().view(np.uint32), case["lat"].view(np.uint32)), anchor_pinned
-            assert np.array_equal(draft.numpy(), case["draft"]), anchor_pinned
+            assert np.array_equal(lat.numpy().view(np.uint32), case["lat"].view(np.uint32)), (hidden_pinned,
+                                                                                               anchor_pinned)
+            assert np.array_equal(draft.numpy(), case["draft"]), (hidden_pinned, anchor_pinned)
     # new anchors written in place reach the next call on the direct path
+    h_hidden = torch.from_numpy(x["hidden"].view(np.int16)).view(torch.bfloat16).pin_memory()
     h_anchor = torch.from_numpy(x["anchor"].copy()).pin_memory()
     plan = df.SelectHostPlan(h_hidden, d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], h_anchor, cfg.k, cfg.T,
                              workspace=hw)
