@@ -15,6 +15,19 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
+// Order-preserving map of a float to an unsigned key (larger float, larger key); every key
+// of a float is above 0, which marks an empty bound slot.
+__device__ __forceinline__ uint32_t bound_key(float x)
+{
+    const uint32_t u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float bound_value(uint32_t key)
+{
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // One CTA per (row, column slice), 8 warps.  Each warp keeps one warp-wide sorted list
 // (lane j holds entry j) over a contiguous part of the slice: lanes load 16-byte groups
 // (8 in flight per lane); a group of 128 values is offered to the list only when one of
@@ -22,6 +35,11 @@ constexpr int kWarps = kThreads / 32;
 // the lanes holding such values insert (a per-thread list would diverge: some lane of the
 // warp would insert on almost every step).  A bitonic butterfly then merges the 8 warp
 // lists into the slice's partial list.
+// The warps share a lower bound: warp w keeps its best S/8 entries in shared-memory slots
+// (S = max(KP, 8), as order-preserving keys), so the slots hold values of S distinct
+// columns and their minimum is a lower bound on the slice's KP-th best value.  A value
+// below it is outranked by KP others and cannot reach the row's top-k, so each warp skips
+// it: the warps warm up together instead of each on its own eighth of the slice.
 template <int KP, bool kVec4>
 __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const float *__restrict__ logits, int V,
                                                                        int n_split, float *__restrict__ pval,
@@ -34,6 +52,12 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
     const float *row = logits + static_cast<long long>(r) * V;
     WarpList wl;
     wl.init();
+    constexpr int kSlots = KP > kWarps ? KP : kWarps;
+    constexpr int kPerWarp = kSlots / kWarps;
+    __shared__ uint32_t s_slot[kSlots];
+    if (threadIdx.x < kSlots)
+        s_slot[threadIdx.x] = 0u;  // empty: no bound yet
+    __syncthreads();
     if constexpr (kVec4) {
         const int groups = V / 4;
         const int g0 = static_cast<int>(static_cast<long long>(s) * groups / n_split);
@@ -45,6 +69,10 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
         float thr = -INFINITY;  // the list's KP-th entry (warp-uniform)
         int thr_i = INT_MAX;
         for (int g = w0 + lane; g < w1 + lane; g += 32 * kU) {
+            // the shared bound: values below it are skipped, values equal to it still pass
+            const uint32_t key = lane < kSlots ? reinterpret_cast<volatile uint32_t *>(s_slot)[lane] : 0xffffffffu;
+            const uint32_t kmin = __reduce_min_sync(kFullMask, key);
+            const float bound = kmin == 0u ? -INFINITY : bound_value(kmin);
             float4 x[kU];
 #pragma unroll
             for (int u = 0; u < kU; ++u) {
@@ -57,14 +85,14 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
                 // a value equal to the KP-th entry ranks after it: only a strictly larger
                 // value can enter, and most groups have none.
                 const float m = fmaxf(fmaxf(x[u].x, x[u].y), fmaxf(x[u].z, x[u].w));
-                if (__any_sync(kFullMask, m > thr)) {
+                if (__any_sync(kFullMask, m > thr && m >= bound)) {
                     // ids of the group: 4 * (base + lane) + component, base warp-uniform
                     const int base = g - lane + 32 * u;
                     const float xc[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         // >= keeps every value that may enter; ranks_before decides exactly
-                        unsigned cand = __ballot_sync(kFullMask, xc[c] >= thr);
+                        unsigned cand = __ballot_sync(kFullMask, xc[c] >= thr && xc[c] >= bound);
                         while (cand) {
                             const int src = __ffs(cand) - 1;
                             cand &= cand - 1u;
@@ -74,6 +102,9 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
                                 wl.insert(cv, ci);
                                 thr = __shfl_sync(kFullMask, wl.v, KP - 1);
                                 thr_i = __shfl_sync(kFullMask, wl.i, KP - 1);
+                                if (lane < kPerWarp)  // this warp's best entries, in its own slots
+                                    reinterpret_cast<volatile uint32_t *>(s_slot)[warp * kPerWarp + lane] =
+                                        bound_key(wl.v);
                             }
                         }
                     }
