@@ -207,7 +207,7 @@ df2_status select_checked(const df2_dims &d, const void *hidden, const void *W_v
     int n_split = 0;
     DF2_CUDA(profile_mark(t_profile_begin, st));
     DF2_CUDA(launch_lm_head(hidden, R, d.H, W_vocab, d.V, kp, w.pval, w.pid, &n_split, W_sel, d.D, g, d.D, w.bound,
-                            w.group_done, w.status, st));
+                            w.group_done, w.status, true, st));
     DF2_CUDA(profile_mark(t_profile_end, st));
     HostMirrors m = mirrors;
     m.status_dev = w.status;

@@ -60,6 +60,10 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
     __shared__ float s_unary[32];
     __shared__ int s_last;
 
+    // the next call's LM head may start now: it prefetches weights and waits for this grid
+    // before it touches anything this kernel reads
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
     const int r = blockIdx.x;
     const int b = r / a.T;
     const int t = r - b * a.T;

@@ -490,6 +490,41 @@ def test_select_leaves_control_block_zero(B, T, H, V, k):
     assert np.array_equal(lat_a.view(np.uint32), lat_a2.view(np.uint32)) and np.array_equal(draft_a, draft_a2)
 
 
+@pytest.mark.parametrize("B,T,H,V,k", [(1, 16, 512, 30000, 8), (20, 16, 256, 20000, 16)])
+def test_back_to_back_calls_on_one_workspace(B, T, H, V, k):
+    """Calls enqueued back to back on one workspace, no sync between: each call's LM head starts
+    under the previous call's finish kernel and must not disturb what that kernel still reads."""
+    D = 64
+    cfg, xa = small_case(B, T, H, V, k, D, seed=B * T + 5)
+    _, xb = small_case(B, T, H, V, k, D, seed=B * T + 6)
+    dims = df.make_dims(B, T, H, V, k, D)
+    common = {n: dev_bf16(xa[n]) for n in ("W_vocab", "W_sel", "pred_cb", "succ_cb")}
+    ha, hb = dev_bf16(xa["hidden"]), dev_bf16(xb["hidden"])
+    aa, ab = dev(xa["anchor"]), dev(xb["anchor"])
+
+    def call(h, an, ws, lat, dr):
+        df.dflash2_select(h, common["W_vocab"], common["W_sel"], common["pred_cb"], common["succ_cb"], an, k, T,
+                          lattice=lat, draft_ids=dr, workspace=ws)
+
+    R = B * T
+    new = lambda: (torch.empty((R, k + k * k), device="cuda"), torch.empty((B, T), dtype=torch.int32, device="cuda"))
+    ref_a, ref_b = new(), new()
+    call(ha, aa, df.Workspace(dims), *ref_a)
+    torch.cuda.synchronize()
+    call(hb, ab, df.Workspace(dims), *ref_b)
+    torch.cuda.synchronize()
+    ws = df.Workspace(dims)
+    outs = [new() for _ in range(6)]
+    for i, o in enumerate(outs):
+        call(ha if i % 2 == 0 else hb, aa if i % 2 == 0 else ab, ws, *o)
+    torch.cuda.synchronize()
+    df.dflash2_check_device_status(ws)
+    for i, (lat, dr) in enumerate(outs):
+        ref = ref_a if i % 2 == 0 else ref_b
+        assert torch.equal(lat.view(torch.int32), ref[0].view(torch.int32)), i
+        assert torch.equal(dr, ref[1]), i
+
+
 def test_zeroed_codebooks_give_per_position_top1():
     cfg, x = small_case(4, 6, 256, 2048, 8, 32, seed=5)
     x["pred_cb"][:] = 0
