@@ -51,6 +51,73 @@ struct FinishArgs {
 
 constexpr int kFinishThreads = 128;
 
+// Bitonic sort of one (value, id) pair per lane across the warp: lane j ends with the j-th
+// pair in (value desc, id asc) order.
+__device__ __forceinline__ void warp_sort_desc(float &v, int &i)
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float ov = __shfl_xor_sync(kFullMask, v, stride);
+            const int oi = __shfl_xor_sync(kFullMask, i, stride);
+            // the lower lane of a pair keeps the better pair where this block runs descending
+            const bool keep_better = ((lane & stride) == 0) == ((lane & size) == 0);
+            if (keep_better == ranks_before(ov, oi, v, i)) {
+                v = ov;
+                i = oi;
+            }
+        }
+    }
+}
+
+// The row's top-KP from the lanes' sorted local lists (av, ai) without the warp butterfly.
+// The KP-th best of the 32 lane heads, tau, is outranked or matched by at least KP entries,
+// so every entry of the row's top-KP ranks at or before it; when at most 32 entries do,
+// they are gathered in shared memory (`sv`, `si`: 32 slots) and sorted across the warp, and
+// lane j receives the j-th best.  Returns false (nothing changed) when more than 32 entries
+// rank at or before tau; the caller then merges with the butterfly.  Warp-uniform.
+template <int KP>
+__device__ __forceinline__ bool bounded_merge(const float (&av)[KP], const int (&ai)[KP], float *sv, int *si,
+                                              float &out_v, int &out_i)
+{
+    const int lane = threadIdx.x & 31;
+    float hv = av[0];
+    int hi = ai[0];
+    warp_sort_desc(hv, hi);
+    const float tv = __shfl_sync(kFullMask, hv, KP - 1);
+    const int ti = __shfl_sync(kFullMask, hi, KP - 1);
+    int n = 0;  // entries of this lane's list at or before tau (a prefix: the list is sorted)
+#pragma unroll
+    for (int j = 0; j < KP; ++j)
+        n += ranks_before(tv, ti, av[j], ai[j]) ? 0 : 1;
+    int incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int up = __shfl_up_sync(kFullMask, incl, o);
+        if (lane >= o)
+            incl += up;
+    }
+    const int total = __shfl_sync(kFullMask, incl, 31);
+    if (total > 32)
+        return false;
+    const int off = incl - n;
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+        if (j < n) {
+            sv[off + j] = av[j];
+            si[off + j] = ai[j];
+        }
+    }
+    __syncwarp();
+    out_v = lane < total ? sv[lane] : -INFINITY;
+    out_i = lane < total ? si[lane] : INT_MAX;
+    __syncwarp();
+    warp_sort_desc(out_v, out_i);
+    return true;
+}
+
 template <int KP>
 __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs a)
 {
@@ -59,6 +126,8 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
     __shared__ int s_prev[32];
     __shared__ float s_unary[32];
     __shared__ int s_last;
+    __shared__ float s_mv[2][32];  // bounded-merge gathers, one per merging warp
+    __shared__ int s_mi[2][32];
 
     // the next call's LM head may start now: it prefetches weights and waits for this grid
     // before it touches anything this kernel reads
@@ -117,16 +186,31 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
             for (int u = 0; u < kLists; ++u)
                 merge_top<KP>(av, ai, bv[u], bi[u]);
         }
-        warp_merge_top<KP>(av, ai, 31);
-        if (lane == 0) {
+        // the lanes' lists into the row's top-k: the bounded merge (measured on GB300 at 512
+        // rows, k = 16: far fewer instructions than the butterfly), else the butterfly
+        float mv;
+        int mi;
+        if (KP <= 16 && bounded_merge<KP>(av, ai, s_mv[warp], s_mi[warp], mv, mi)) {
+            if (lane < k) {
+                if (warp == 0) {
+                    s_cand[lane] = clamp_id(mi, a.V);
+                    s_unary[lane] = mv;
+                } else {
+                    s_prev[lane] = clamp_id(mi, a.V);
+                }
+            }
+        } else {
+            warp_merge_top<KP>(av, ai, 31);
+            if (lane == 0) {
 #pragma unroll
-            for (int s = 0; s < KP; ++s) {
-                if (s < k) {
-                    if (warp == 0) {
-                        s_cand[s] = clamp_id(ai[s], a.V);
-                        s_unary[s] = av[s];
-                    } else {
-                        s_prev[s] = clamp_id(ai[s], a.V);
+                for (int s = 0; s < KP; ++s) {
+                    if (s < k) {
+                        if (warp == 0) {
+                            s_cand[s] = clamp_id(ai[s], a.V);
+                            s_unary[s] = av[s];
+                        } else {
+                            s_prev[s] = clamp_id(ai[s], a.V);
+                        }
                     }
                 }
             }
