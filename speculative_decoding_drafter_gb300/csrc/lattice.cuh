@@ -34,6 +34,35 @@ __host__ __device__ constexpr size_t lattice_smem_bytes(int k, int D)
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// float32 -> tf32 (round to nearest, ties away), as the bit pattern an mma operand takes.
+__device__ __forceinline__ uint32_t to_tf32(float x)
+{
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D (16 x 8, float32) += A (16 x 8, tf32, row-major) . B (8 x 8, tf32, column-major), one warp.
+// Fragments (g = lane / 4, c = lane % 4): a = A[g][c], A[g+8][c], A[g][c+4], A[g+8][c+4];
+// b = B[c][g], B[c+4][g]; d = D[g][2c], D[g][2c+1], D[g+8][2c], D[g+8][2c+1].
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Rows of the lattice whose scores come from warp-level tensor-core tiles: 9 to 16
+// predecessors and candidates (one 16 x 16 tile), with room in the gathered-row buffer for
+// four 16 x 17 float partial tiles once the products are done.  Measured on GB300: 24.5 ->
+// 23.0 us after the LM head at 512 rows (k = 16); at k = 8 the scalar path's latency is as
+// low (12.6 vs 13.1 us at batch 1), so smaller k keep it.
+__host__ __device__ constexpr bool lattice_uses_mma(int k, int n_prev, int D)
+{
+    return k > 8 && k <= 16 && n_prev == k && 2 * k * D * 2 >= 4 * 16 * 17 * 4;
+}
+
 // Copies the gate row g[0..D) into shared memory (threads [first, first + count) of the CTA).
 __device__ __forceinline__ void load_gate_row(float *sg, const float *__restrict__ g, int D, int first, int count)
 {
@@ -106,70 +135,134 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
     }
     __syncthreads();
 
-    // Each warp takes two predecessor rows at a time; lanes stride over pairs of d.
-    const uint32_t *succ2 = reinterpret_cast<const uint32_t *>(rows + n_prev * D);  // [k][D/2]
-    const float2 *g2 = reinterpret_cast<const float2 *>(sg);
-    const int D2 = D / 2;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n_warps = blockDim.x >> 5;
-    for (int i0 = 2 * warp; i0 < n_prev; i0 += 2 * n_warps) {
-        const bool two = i0 + 1 < n_prev;
-        const uint32_t *a0 = reinterpret_cast<const uint32_t *>(rows + i0 * D);
-        const uint32_t *a1 = two ? a0 + D2 : a0;
-        float acc0[KP], acc1[KP];
-#pragma unroll
-        for (int j = 0; j < KP; ++j) {
-            acc0[j] = 0.f;
-            acc1[j] = 0.f;
+    // writes score row i (lane j: unary_j + tot) and, if asked, the walk's choice from it
+    auto emit_row = [&](int i, float tot) {
+        const float s = lane < k ? s_unary[lane] + tot : -INFINITY;
+        if (lane < k) {
+            if (n_prev == 1) {
+                for (int ii = 0; ii < k; ++ii) {
+                    out[k + ii * k + lane] = s;
+                    if (mirror)
+                        mirror[k + ii * k + lane] = s;
+                }
+            } else {
+                out[k + i * k + lane] = s;
+                if (mirror)
+                    mirror[k + i * k + lane] = s;
+            }
         }
-        for (int d2 = lane; d2 < D2; d2 += 32) {
-            const float2 gg = g2[d2];
-            const uint32_t p0 = a0[d2], p1 = a1[d2];
-            const float x0 = bf16_lo(p0) * gg.x, y0 = bf16_hi(p0) * gg.y;  // A(prev) (.) g
-            const float x1 = bf16_lo(p1) * gg.x, y1 = bf16_hi(p1) * gg.y;
+        if (best) {
+            float x = s;
+            int j = lane < k ? lane : 0x7fffffff;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ox = __shfl_xor_sync(kFullMask, x, off);
+                const int oj = __shfl_xor_sync(kFullMask, j, off);
+                const bool take = ranks_before(ox, oj, x, j);
+                x = take ? ox : x;
+                j = take ? oj : j;
+            }
+            if (lane == 0)
+                best[i] = j;
+        }
+    };
+
+    if (KP <= 16 && lattice_uses_mma(k, n_prev, D)) {
+        // Scores as one 16 x 16 tile of warp-level tf32 tensor-core products, the K = D axis
+        // split over up to 4 warps: A = A(prev) (.) g is split into tf32 high and low parts
+        // and B(cand) is bf16 (exact in tf32), so the two products keep float32 accuracy.
+        const int mw = n_warps < 4 ? n_warps : 4;
+        const int gq = lane >> 2, cq = lane & 3;
+        float acc[2][2][4] = {};  // [high / low part][candidate tile][fragment]
+        if (warp < mw) {
+            const bool va0 = gq < n_prev, va1 = gq + 8 < n_prev;
+            const bool vb0 = gq < k, vb1 = gq + 8 < k;
+            const uint16_t *pa0 = rows + (va0 ? gq : 0) * D;
+            const uint16_t *pa1 = rows + (va1 ? gq + 8 : 0) * D;
+            const uint16_t *pb0 = rows + (n_prev + (vb0 ? gq : 0)) * D;
+            const uint16_t *pb1 = rows + (n_prev + (vb1 ? gq + 8 : 0)) * D;
+            for (int k0 = warp * 8; k0 < D; k0 += mw * 8) {
+                const int d0 = k0 + cq, d1 = k0 + cq + 4;
+                const float g0 = sg[d0], g1 = sg[d1];
+                float p[4];
+                p[0] = va0 ? __uint_as_float(static_cast<uint32_t>(pa0[d0]) << 16) * g0 : 0.f;
+                p[1] = va1 ? __uint_as_float(static_cast<uint32_t>(pa1[d0]) << 16) * g0 : 0.f;
+                p[2] = va0 ? __uint_as_float(static_cast<uint32_t>(pa0[d1]) << 16) * g1 : 0.f;
+                p[3] = va1 ? __uint_as_float(static_cast<uint32_t>(pa1[d1]) << 16) * g1 : 0.f;
+                uint32_t ahi[4], alo[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    ahi[q] = to_tf32(p[q]);
+                    alo[q] = to_tf32(p[q] - __uint_as_float(ahi[q]));
+                }
+                const uint32_t b00 = vb0 ? static_cast<uint32_t>(pb0[d0]) << 16 : 0u;
+                const uint32_t b01 = vb0 ? static_cast<uint32_t>(pb0[d1]) << 16 : 0u;
+                const uint32_t b10 = vb1 ? static_cast<uint32_t>(pb1[d0]) << 16 : 0u;
+                const uint32_t b11 = vb1 ? static_cast<uint32_t>(pb1[d1]) << 16 : 0u;
+                mma_tf32_16x8x8(acc[0][0], ahi, b00, b01);
+                mma_tf32_16x8x8(acc[0][1], ahi, b10, b11);
+                mma_tf32_16x8x8(acc[1][0], alo, b00, b01);
+                mma_tf32_16x8x8(acc[1][1], alo, b10, b11);
+            }
+        }
+        __syncthreads();  // every warp is done with the gathered rows: reuse them for the partial tiles
+        float(*part)[16][17] = reinterpret_cast<float(*)[16][17]>(rows);
+        if (warp < mw) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int col = nt * 8 + 2 * cq;
+                part[warp][gq][col] = acc[0][nt][0] + acc[1][nt][0];
+                part[warp][gq][col + 1] = acc[0][nt][1] + acc[1][nt][1];
+                part[warp][gq + 8][col] = acc[0][nt][2] + acc[1][nt][2];
+                part[warp][gq + 8][col + 1] = acc[0][nt][3] + acc[1][nt][3];
+            }
+        }
+        __syncthreads();
+        for (int i = warp; i < n_prev; i += n_warps) {
+            float tot = 0.f;
+            if (lane < k)
+                for (int w = 0; w < mw; ++w)
+                    tot += part[w][i][lane];
+            emit_row(i, tot);
+        }
+    } else {
+        // Each warp takes two predecessor rows at a time; lanes stride over pairs of d.
+        const uint32_t *succ2 = reinterpret_cast<const uint32_t *>(rows + n_prev * D);  // [k][D/2]
+        const float2 *g2 = reinterpret_cast<const float2 *>(sg);
+        const int D2 = D / 2;
+        for (int i0 = 2 * warp; i0 < n_prev; i0 += 2 * n_warps) {
+            const bool two = i0 + 1 < n_prev;
+            const uint32_t *a0 = reinterpret_cast<const uint32_t *>(rows + i0 * D);
+            const uint32_t *a1 = two ? a0 + D2 : a0;
+            float acc0[KP], acc1[KP];
 #pragma unroll
             for (int j = 0; j < KP; ++j) {
-                if (j < k) {
-                    const uint32_t sb = succ2[j * D2 + d2];
-                    const float sl = bf16_lo(sb), sh = bf16_hi(sb);
-                    acc0[j] = fmaf(y0, sh, fmaf(x0, sl, acc0[j]));
-                    acc1[j] = fmaf(y1, sh, fmaf(x1, sl, acc1[j]));
-                }
+                acc0[j] = 0.f;
+                acc1[j] = 0.f;
             }
-        }
-        const float tot0 = warp_reduce_scatter<KP>(acc0);
-        const float tot1 = warp_reduce_scatter<KP>(acc1);
-        for (int h = 0; h < (two ? 2 : 1); ++h) {
-            const int i = i0 + h;
-            const float s = lane < k ? s_unary[lane] + (h == 0 ? tot0 : tot1) : -INFINITY;
-            if (lane < k) {
-                if (n_prev == 1) {
-                    for (int ii = 0; ii < k; ++ii) {
-                        out[k + ii * k + lane] = s;
-                        if (mirror)
-                            mirror[k + ii * k + lane] = s;
-                    }
-                } else {
-                    out[k + i * k + lane] = s;
-                    if (mirror)
-                        mirror[k + i * k + lane] = s;
-                }
-            }
-            if (best) {
-                float x = s;
-                int j = lane < k ? lane : 0x7fffffff;
+            for (int d2 = lane; d2 < D2; d2 += 32) {
+                const float2 gg = g2[d2];
+                const uint32_t p0 = a0[d2], p1 = a1[d2];
+                const float x0 = bf16_lo(p0) * gg.x, y0 = bf16_hi(p0) * gg.y;  // A(prev) (.) g
+                const float x1 = bf16_lo(p1) * gg.x, y1 = bf16_hi(p1) * gg.y;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ox = __shfl_xor_sync(kFullMask, x, off);
-                    const int oj = __shfl_xor_sync(kFullMask, j, off);
-                    const bool take = ranks_before(ox, oj, x, j);
-                    x = take ? ox : x;
-                    j = take ? oj : j;
+                for (int j = 0; j < KP; ++j) {
+                    if (j < k) {
+                        const uint32_t sb = succ2[j * D2 + d2];
+                        const float sl = bf16_lo(sb), sh = bf16_hi(sb);
+                        acc0[j] = fmaf(y0, sh, fmaf(x0, sl, acc0[j]));
+                        acc1[j] = fmaf(y1, sh, fmaf(x1, sl, acc1[j]));
+                    }
                 }
-                if (lane == 0)
-                    best[i] = j;
             }
+            const float tot0 = warp_reduce_scatter<KP>(acc0);
+            const float tot1 = warp_reduce_scatter<KP>(acc1);
+            emit_row(i0, tot0);
+            if (two)
+                emit_row(i0 + 1, tot1);
         }
     }
     if (threadIdx.x < k) {
