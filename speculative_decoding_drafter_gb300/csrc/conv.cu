@@ -25,6 +25,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace df2 {
 namespace {
@@ -306,6 +307,12 @@ __global__ void __launch_bounds__(kThreads) dynamic_conv_kernel(const ConvArgs a
     extern __shared__ __align__(16) uint8_t smem[];  // one tile buffer
     __shared__ float s_part[kThreads / 32][kRows + 1];
     __shared__ float s_scale[kRows + 1];
+    // Launched as a programmatic dependent: the next launch's CTAs may take the slots this
+    // grid's last wave frees, and each waits for the grid before it before reading inputs or
+    // writing the output (a back-to-back call writes the same rows).
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();
     stage_tile<kRows>(a, blockIdx.x, smem);
     cp_async_commit_and_wait_all();
     __syncthreads();  // every thread's copies are visible
@@ -328,7 +335,19 @@ cudaError_t launch_rows(ConvArgs a, cudaStream_t stream)
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    dynamic_conv_kernel<kRows><<<static_cast<unsigned>(a.n_tiles), kThreads, smem, stream>>>(a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.n_tiles));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, dynamic_conv_kernel<kRows>, a);
+    if (le != cudaSuccess)
+        return le;
     return cudaGetLastError();
 }
 
