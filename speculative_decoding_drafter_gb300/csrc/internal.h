@@ -98,6 +98,27 @@ cudaError_t launch_dynamic_conv(int B, int T, int C, int G, const uint16_t *x, c
 // Greedy walk, one warp per sequence: draft_ids [B, T].
 cudaError_t launch_walk(int B, int T, int k, const float *lattice, int32_t *draft_ids, cudaStream_t stream);
 
+// Launches `kernel` as a programmatic dependent of the kernel before it on `stream`: it may
+// start under that kernel's tail, and must wait for it (griddep_wait in every CTA, before
+// anything it reads or writes) so that its own completion still implies that kernel's.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // selftest.cu
 cudaError_t launch_wait_selftest(uint32_t *status, unsigned long long limit_ns, cudaStream_t stream);
 

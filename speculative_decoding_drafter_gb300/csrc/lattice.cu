@@ -4,6 +4,7 @@
 
 #include "internal.h"
 #include "lattice.cuh"
+#include "ptx.cuh"
 
 namespace df2 {
 namespace {
@@ -43,6 +44,9 @@ __global__ void __launch_bounds__(kLatticeThreads) lattice_kernel(int T, int k, 
 __global__ void __launch_bounds__(kLatticeThreads) walk_kernel(int B, int T, int k, const float *__restrict__ lattice,
                                                                int32_t *__restrict__ draft)
 {
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();  // launched as a programmatic dependent
     const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
     if (b >= B)
         return;
@@ -62,6 +66,9 @@ __global__ void __launch_bounds__(kLatticeThreads)
                        const float *__restrict__ uniforms, int32_t *__restrict__ draft, int32_t *__restrict__ n_draft,
                        float *__restrict__ confidence)
 {
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();  // launched as a programmatic dependent
     const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (b >= B)
@@ -159,9 +166,8 @@ cudaError_t launch_lattice(int B, int T, int k, int V, int D, const int32_t *top
 
 cudaError_t launch_walk(int B, int T, int k, const float *lattice, int32_t *draft_ids, cudaStream_t stream)
 {
-    walk_kernel<<<static_cast<unsigned>((B + kWarps - 1) / kWarps), kLatticeThreads, 0, stream>>>(B, T, k, lattice,
-                                                                                                  draft_ids);
-    return cudaGetLastError();
+    return launch_dependent(walk_kernel, dim3(static_cast<unsigned>((B + kWarps - 1) / kWarps)), dim3(kLatticeThreads),
+                            0, stream, B, T, k, lattice, draft_ids);
 }
 
 }  // namespace df2
@@ -172,9 +178,9 @@ cudaError_t launch_walk_sample(int B, int T, int k, const float *lattice, float 
                                const float *uniforms, int32_t *draft_ids, int32_t *n_draft, float *confidence,
                                cudaStream_t stream)
 {
-    walk_sample_kernel<<<static_cast<unsigned>((B + kWarps - 1) / kWarps), kLatticeThreads, 0, stream>>>(
-        B, T, k, lattice, temperature, p_min, uniforms, draft_ids, n_draft, confidence);
-    return cudaGetLastError();
+    return launch_dependent(walk_sample_kernel, dim3(static_cast<unsigned>((B + kWarps - 1) / kWarps)),
+                            dim3(kLatticeThreads), 0, stream, B, T, k, lattice, temperature, p_min, uniforms,
+                            draft_ids, n_draft, confidence);
 }
 
 }  // namespace df2

@@ -7,6 +7,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 #include "topk.cuh"
 
 namespace df2 {
@@ -45,6 +46,9 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
                                                                        int n_split, float *__restrict__ pval,
                                                                        int32_t *__restrict__ pid)
 {
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();  // launched as a programmatic dependent
     const int r = blockIdx.x;
     const int s = blockIdx.y;
     const int warp = threadIdx.x >> 5;
@@ -155,6 +159,9 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float *__res
                                                               int k, int32_t *__restrict__ ids,
                                                               float *__restrict__ vals)
 {
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();  // launched as a programmatic dependent
     const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= R)
@@ -189,10 +196,10 @@ cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32
     const dim3 grid(static_cast<unsigned>(R), static_cast<unsigned>(n_split));
     const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
     if (vec4)
-        logits_topk_partial_kernel<KP, true><<<grid, kThreads, 0, stream>>>(logits, V, n_split, pval, pid);
-    else
-        logits_topk_partial_kernel<KP, false><<<grid, kThreads, 0, stream>>>(logits, V, n_split, pval, pid);
-    return cudaGetLastError();
+        return launch_dependent(logits_topk_partial_kernel<KP, true>, grid, dim3(kThreads), 0, stream, logits, V,
+                                n_split, pval, pid);
+    return launch_dependent(logits_topk_partial_kernel<KP, false>, grid, dim3(kThreads), 0, stream, logits, V, n_split,
+                            pval, pid);
 }
 
 }  // namespace
@@ -213,8 +220,8 @@ cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int 
                               int32_t *topk_ids, float *topk_vals, cudaStream_t stream)
 {
     const dim3 grid(static_cast<unsigned>((R + kWarps - 1) / kWarps));
-    topk_merge_kernel<<<grid, kThreads, 0, stream>>>(pval, pid, R, n_split * KP, k, topk_ids, topk_vals);
-    return cudaGetLastError();
+    return launch_dependent(topk_merge_kernel, grid, dim3(kThreads), 0, stream, pval, pid, R, n_split * KP, k,
+                            topk_ids, topk_vals);
 }
 
 }  // namespace df2
