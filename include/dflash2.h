@@ -31,7 +31,10 @@
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
  *    the legacy default stream).  The returned status covers argument
  *    validation and launch errors (cudaGetLastError after enqueue); it does
- *    not wait for the kernels.
+ *    not wait for the kernels.  Some kernels are launched as programmatic
+ *    dependents: they may begin under the tail of the kernel before them on
+ *    the stream, but read their inputs and write their outputs only after it
+ *    has completed, so stream order holds as for ordinary launches.
  *  - bf16 tensors are IEEE bfloat16, row-major and contiguous.  Tensors read
  *    by the tensor-memory-accelerator or by 16-byte vector loads (hidden,
  *    W_vocab, W_sel, pred_cb, succ_cb, logits) must be 16-byte aligned; the
