@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                 const Chunk ch = chunk_of(args, slice, c);
                 const CUtensorMap *wide = ch.store ? &map_s_wide : &map_t_wide;
                 const CUtensorMap *narrow = ch.store ? &map_s_narrow : &map_t_narrow;
-                const uint32_t tx = static_cast<uint32_t>(kbs * (tiles * args.a_bytes + ch.n * BK * 2));
+                // with two tiles one 256-row box brings both A tiles (rows past R read zeros)
+                const uint32_t tx = static_cast<uint32_t>(kbs * ((MT == 2 ? 2 : tiles) * args.a_bytes + ch.n * BK * 2));
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -284,9 +285,8 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                     mbar_arrive_expect_tx(full_bar(stage), tx);
                     for (int q = 0; q < kbs; ++q) {
                         const int x = (ks * kbs + q) * BK;  // past K the boxes read zeros
-                        for (int t = 0; t < tiles; ++t)
-                            tma_load_2d(smem_u32(st + (q * mt + t) * args.a_bytes), &map_a, full_bar(stage), x,
-                                        (tile0 + t) * BM);
+                        // the group's tiles are adjacent rows of A and adjacent in shared memory: one box
+                        tma_load_2d(smem_u32(st + q * mt * args.a_bytes), &map_a, full_bar(stage), x, tile0 * BM);
                         const uint32_t b_dst = smem_u32(st + kbs * mt * args.a_bytes + q * b_sub);
                         // the weights stream through once: evict-first in L2 (measured on GB300:
                         // 197.3 vs 198.0 us at 16 rows, 248.3 vs 250.0 at 64, 449.9 vs 455.1 at 512)
@@ -599,7 +599,8 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
 
     CUtensorMap ma, mtw, mtn, msw, msn;
     cudaError_t e;
-    if ((e = make_map(&ma, A, K, R, a_rows)) != cudaSuccess)
+    // two row tiles per CTA: one box covers both (256 rows, the largest TMA box)
+    if ((e = make_map(&ma, A, K, R, args.mt == 2 ? 2 * a_rows : a_rows)) != cudaSuccess)
         return e;
     // an empty segment gets the other segment's maps (never read)
     const void *tb = n_topk > 0 ? Bt : Bs;
