@@ -275,7 +275,11 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                 const CUtensorMap *wide = ch.store ? &map_s_wide : &map_t_wide;
                 const CUtensorMap *narrow = ch.store ? &map_s_narrow : &map_t_narrow;
                 // with two tiles one 256-row box brings both A tiles (rows past R read zeros)
-                const uint32_t tx = static_cast<uint32_t>(kbs * ((MT == 2 ? 2 : tiles) * args.a_bytes + ch.n * BK * 2));
+                // With two tiles (bound by TMA operations, not bytes) a narrow chunk's B rows come
+                // in one full-width box too: the rows past the chunk are W's next rows or zeros
+                // past its end, and the MMA reads only the chunk's n.
+                const int b_rows = MT == 2 ? args.bn : ch.n;
+                const uint32_t tx = static_cast<uint32_t>(kbs * ((MT == 2 ? 2 : tiles) * args.a_bytes + b_rows * BK * 2));
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                         const uint32_t b_dst = smem_u32(st + kbs * mt * args.a_bytes + q * b_sub);
                         // the weights stream through once: evict-first in L2 (measured on GB300:
                         // 197.3 vs 198.0 us at 16 rows, 248.3 vs 250.0 at 64, 449.9 vs 455.1 at 512)
-                        if (ch.n == args.bn) {
+                        if (ch.n == args.bn || MT == 2) {
                             tma_load_2d_policy(b_dst, wide, full_bar(stage), x, ch.b_row, stream_policy);
                         } else {
                             for (int u = 0; u < ch.n / UNIT; ++u)
