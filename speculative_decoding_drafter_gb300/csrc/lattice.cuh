@@ -24,11 +24,21 @@ __device__ __forceinline__ int clamp_id(int id, int V)
     return static_cast<unsigned>(id) < static_cast<unsigned>(V) ? id : 0;
 }
 
+// Elements between consecutive gathered codebook rows in shared memory: D plus 16 bytes, so
+// that the eight rows one tensor-core fragment load touches start in eight different groups of
+// four banks (with a stride of D alone every row starts in bank 0 whenever D is a multiple of 64).
+__host__ __device__ constexpr int lattice_row_stride(int D)
+{
+    return D + 8;
+}
+
 // Dynamic shared memory of one lattice row: the gate row as float [D], then the gathered
-// codebook rows as bf16: up to k predecessor rows A(prev_i) followed by k rows B(cand_j).
+// codebook rows as bf16: up to k predecessor rows A(prev_i) followed by k rows B(cand_j), each
+// lattice_row_stride(D) elements apart.
 __host__ __device__ constexpr size_t lattice_smem_bytes(int k, int D)
 {
-    return sizeof(float) * static_cast<size_t>(D) + sizeof(uint16_t) * 2 * static_cast<size_t>(k) * D;
+    return sizeof(float) * static_cast<size_t>(D) +
+           sizeof(uint16_t) * 2 * static_cast<size_t>(k) * lattice_row_stride(D);
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -109,7 +119,8 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
 {
     constexpr int kBatch = 8;  // 16-byte gathers in flight per thread
     const float *sg = reinterpret_cast<const float *>(smem);                  // [D] gate
-    uint16_t *rows = reinterpret_cast<uint16_t *>(smem + sizeof(float) * D);  // [n_prev + k][D]
+    uint16_t *rows = reinterpret_cast<uint16_t *>(smem + sizeof(float) * D);  // [n_prev + k][ld]
+    const int ld = lattice_row_stride(D);
     __syncthreads();
     const int chunks = D / 8;  // 16-byte chunks of bf16 per codebook row
     const int total = (n_prev + k) * chunks;
@@ -129,8 +140,10 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
             const int idx = base + q * blockDim.x;
-            if (idx < total)
-                reinterpret_cast<uint4 *>(rows)[idx] = w[q];
+            if (idx < total) {
+                const int row = idx / chunks;
+                reinterpret_cast<uint4 *>(rows + row * ld)[idx - row * chunks] = w[q];
+            }
         }
     }
     __syncthreads();
@@ -170,38 +183,44 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
         }
     };
 
-    if (KP <= 16 && lattice_uses_mma(k, n_prev, D)) {
+    if (KP > 8 && KP <= 16 && lattice_uses_mma(k, n_prev, D)) {  // k <= KP: no tile below KP = 16
         // Scores as one 16 x 16 tile of warp-level tf32 tensor-core products, the K = D axis
         // split over up to 4 warps: A = A(prev) (.) g is split into tf32 high and low parts
         // and B(cand) is bf16 (exact in tf32), so the two products keep float32 accuracy.
+        // The order of the K axis inside an 8-wide step is free as long as A and B agree:
+        // fragment columns c and c + 4 take d = k0 + 2c and k0 + 2c + 1, the two halves of one
+        // 32-bit word of each row, so a thread reads one word per row and step.
         const int mw = n_warps < 4 ? n_warps : 4;
         const int gq = lane >> 2, cq = lane & 3;
+        const int ld2 = ld / 2;
         float acc[2][2][4] = {};  // [high / low part][candidate tile][fragment]
         if (warp < mw) {
             const bool va0 = gq < n_prev, va1 = gq + 8 < n_prev;
             const bool vb0 = gq < k, vb1 = gq + 8 < k;
-            const uint16_t *pa0 = rows + (va0 ? gq : 0) * D;
-            const uint16_t *pa1 = rows + (va1 ? gq + 8 : 0) * D;
-            const uint16_t *pb0 = rows + (n_prev + (vb0 ? gq : 0)) * D;
-            const uint16_t *pb1 = rows + (n_prev + (vb1 ? gq + 8 : 0)) * D;
+            const uint32_t *rw = reinterpret_cast<const uint32_t *>(rows);
+            const uint32_t *pa0 = rw + (va0 ? gq : 0) * ld2;
+            const uint32_t *pa1 = rw + (va1 ? gq + 8 : 0) * ld2;
+            const uint32_t *pb0 = rw + (n_prev + (vb0 ? gq : 0)) * ld2;
+            const uint32_t *pb1 = rw + (n_prev + (vb1 ? gq + 8 : 0)) * ld2;
+            const float2 *g2 = reinterpret_cast<const float2 *>(sg);
             for (int k0 = warp * 8; k0 < D; k0 += mw * 8) {
-                const int d0 = k0 + cq, d1 = k0 + cq + 4;
-                const float g0 = sg[d0], g1 = sg[d1];
+                const int w = k0 / 2 + cq;
+                const float2 gg = g2[w];
+                const uint32_t a0 = va0 ? pa0[w] : 0u, a1 = va1 ? pa1[w] : 0u;
                 float p[4];
-                p[0] = va0 ? __uint_as_float(static_cast<uint32_t>(pa0[d0]) << 16) * g0 : 0.f;
-                p[1] = va1 ? __uint_as_float(static_cast<uint32_t>(pa1[d0]) << 16) * g0 : 0.f;
-                p[2] = va0 ? __uint_as_float(static_cast<uint32_t>(pa0[d1]) << 16) * g1 : 0.f;
-                p[3] = va1 ? __uint_as_float(static_cast<uint32_t>(pa1[d1]) << 16) * g1 : 0.f;
+                p[0] = bf16_lo(a0) * gg.x;
+                p[1] = bf16_lo(a1) * gg.x;
+                p[2] = bf16_hi(a0) * gg.y;
+                p[3] = bf16_hi(a1) * gg.y;
                 uint32_t ahi[4], alo[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     ahi[q] = to_tf32(p[q]);
                     alo[q] = to_tf32(p[q] - __uint_as_float(ahi[q]));
                 }
-                const uint32_t b00 = vb0 ? static_cast<uint32_t>(pb0[d0]) << 16 : 0u;
-                const uint32_t b01 = vb0 ? static_cast<uint32_t>(pb0[d1]) << 16 : 0u;
-                const uint32_t b10 = vb1 ? static_cast<uint32_t>(pb1[d0]) << 16 : 0u;
-                const uint32_t b11 = vb1 ? static_cast<uint32_t>(pb1[d1]) << 16 : 0u;
+                const uint32_t b0 = vb0 ? pb0[w] : 0u, b1 = vb1 ? pb1[w] : 0u;
+                const uint32_t b00 = b0 << 16, b01 = b0 & 0xFFFF0000u;
+                const uint32_t b10 = b1 << 16, b11 = b1 & 0xFFFF0000u;
                 mma_tf32_16x8x8(acc[0][0], ahi, b00, b01);
                 mma_tf32_16x8x8(acc[0][1], ahi, b10, b11);
                 mma_tf32_16x8x8(acc[1][0], alo, b00, b01);
@@ -230,13 +249,13 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
         }
     } else {
         // Each warp takes two predecessor rows at a time; lanes stride over pairs of d.
-        const uint32_t *succ2 = reinterpret_cast<const uint32_t *>(rows + n_prev * D);  // [k][D/2]
+        const uint32_t *succ2 = reinterpret_cast<const uint32_t *>(rows + n_prev * ld);  // [k][ld/2]
         const float2 *g2 = reinterpret_cast<const float2 *>(sg);
-        const int D2 = D / 2;
+        const int D2 = D / 2, ld2 = ld / 2;
         for (int i0 = 2 * warp; i0 < n_prev; i0 += 2 * n_warps) {
             const bool two = i0 + 1 < n_prev;
-            const uint32_t *a0 = reinterpret_cast<const uint32_t *>(rows + i0 * D);
-            const uint32_t *a1 = two ? a0 + D2 : a0;
+            const uint32_t *a0 = reinterpret_cast<const uint32_t *>(rows + i0 * ld);
+            const uint32_t *a1 = two ? a0 + ld2 : a0;
             float acc0[KP], acc1[KP];
 #pragma unroll
             for (int j = 0; j < KP; ++j) {
@@ -251,7 +270,7 @@ __device__ void lattice_row(int k, int D, int n_prev, const int *s_prev, const i
 #pragma unroll
                 for (int j = 0; j < KP; ++j) {
                     if (j < k) {
-                        const uint32_t sb = succ2[j * D2 + d2];
+                        const uint32_t sb = succ2[j * ld2 + d2];
                         const float sl = bf16_lo(sb), sh = bf16_hi(sb);
                         acc0[j] = fmaf(y0, sh, fmaf(x0, sl, acc0[j]));
                         acc1[j] = fmaf(y1, sh, fmaf(x1, sl, acc1[j]));
