@@ -23,6 +23,16 @@
 // Two row tiles per CTA (beyond 128 rows) halve what an SM takes in per MMA flop: 64 KB of
 // A and B per 2 x 128x256x64 block instead of 48 KB per 128x256x64, which is what limits
 // the tensor pipe when all SMs stream.
+// CTA pairs (129 to 512 rows): the two row tiles go to a cluster of two CTAs on two SMs
+// instead.  The even CTA issues tcgen05.mma.cta_group::2 (M = 256); each CTA loads its
+// 128-row A tile and a 128-row box of B at its half of the chunk, both completing on the
+// even CTA's barriers, and the commits arrive on both CTAs' barriers.  An SM then takes in
+// the same bytes per flop as with two tiles in one CTA, but holds one 256-column
+// accumulator per buffer, so the epilogue runs under the next chunk's MMAs.  A stage
+// carries two K-blocks, each operand as one box of a 3-D view of the matrix (64 elements
+// of K x rows x K-block): the feed is bound by the number of TMA operations, and one
+// K-block per stage (four operations per 128x256x64 instead of two) was slower than two
+// tiles in one CTA.
 // Work split: CTA (g, s) owns row group g (mt consecutive row tiles) and a contiguous
 // slice of the columns of both segments (multiples of 16), walked in chunks of <= 256
 // that never straddle the segment boundary.  CTAs sharing a slice are launched next to
@@ -70,7 +80,8 @@ struct GemmArgs {
     int n_store;      // columns of the store segment
     int row_tiles, n_split;
     int mt;           // row tiles per CTA (1 or 2)
-    int row_groups;   // ceil(row_tiles / mt)
+    int pair;         // CTA pairs (clusters of two): one row tile per CTA, M = 256 per pair
+    int row_groups;   // ceil(row_tiles / mt); pairs: row_tiles rounded up to even
     int n_bufs;       // accumulator buffers per row tile (2, or 1 when mt tiles fill TMEM)
     int stages;       // pipeline depth
     int bn;           // columns per chunk (128 or 256)
@@ -178,7 +189,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
 // MT (row tiles per CTA) is a template parameter: with one tile the per-tile loops must
 // vanish at compile time (a loop of one run-time iteration around the TMA and MMA issue cost
 // 3% at 16 rows, measured on GB300).
-template <int KP, int MT>
+template <int KP, int MT, bool PAIR>
 __global__ void __launch_bounds__(64 + MT * BM, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_t_wide,
                    const __grid_constant__ CUtensorMap map_t_narrow, const __grid_constant__ CUtensorMap map_s_wide,
@@ -190,7 +201,8 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
     const int kbs = args.kbs;
     constexpr int mt = MT;
     constexpr int n_bufs = 2 * MT * BN <= TMEM_COLS ? 2 : 1;  // bn = 256 whenever MT = 2
-    const int b_sub = args.bn * BK * 2;  // bytes of one B K-block of a full chunk
+    // bytes of one B K-block of a full chunk (of this CTA's half of it in a pair)
+    const int b_sub = (PAIR ? args.bn / 2 : args.bn) * BK * 2;
     // stage layout: kbs x mt A K-blocks (K-block major), then kbs B K-blocks (every part
     // 1024-byte aligned)
     const int stage_bytes = kbs * (mt * args.a_bytes + b_sub);
@@ -202,6 +214,10 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // in a pair, rank 0 issues the MMAs and owns the barriers both CTAs' loads and
+    // accumulator releases complete on
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const bool issuer = rank == 0u;
     const int group = blockIdx.x % args.row_groups;
     const int tile0 = group * mt;
     const int split = blockIdx.x / args.row_groups;
@@ -225,7 +241,7 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), tiles * BM);
+            mbar_init(tempty_bar(b), PAIR ? 2 * BM : tiles * BM);  // a pair: both CTAs' rows
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
@@ -241,11 +257,18 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // the issuer's barriers are initialised before either CTA signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -279,19 +302,36 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                 // in one full-width box too: the rows past the chunk are W's next rows or zeros
                 // past its end, and the MMA reads only the chunk's n.
                 const int b_rows = MT == 2 ? args.bn : ch.n;
-                const uint32_t tx = static_cast<uint32_t>(kbs * ((MT == 2 ? 2 : tiles) * args.a_bytes + b_rows * BK * 2));
+                // a pair: each CTA loads its A tile and a 128-row box of B at its half of the
+                // chunk (rows past the half are unused), all onto the issuer's barrier
+                const uint32_t tx = PAIR ? static_cast<uint32_t>(2 * kbs * (args.a_bytes + b_sub))
+                                         : static_cast<uint32_t>(kbs * ((MT == 2 ? 2 : tiles) * args.a_bytes +
+                                                                        b_rows * BK * 2));
+                const int b_row = PAIR ? ch.b_row + static_cast<int>(rank) * (ch.n / 2) : ch.b_row;
                 for (int ks = 0; ks < kstages; ++ks) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     uint8_t *st = smem + stage * stage_bytes;
-                    mbar_arrive_expect_tx(full_bar(stage), tx);
+                    const uint32_t fb = PAIR ? mapa_shared(full_bar(stage), 0u) : full_bar(stage);
+                    if (!PAIR || issuer)
+                        mbar_arrive_expect_tx(full_bar(stage), tx);
                     for (int q = 0; q < kbs; ++q) {
                         const int x = (ks * kbs + q) * BK;  // past K the boxes read zeros
                         // the group's tiles are adjacent rows of A and adjacent in shared memory: one box
-                        tma_load_2d(smem_u32(st + q * mt * args.a_bytes), &map_a, full_bar(stage), x, tile0 * BM);
+                        const uint32_t a_dst = smem_u32(st + q * mt * args.a_bytes);
                         const uint32_t b_dst = smem_u32(st + kbs * mt * args.a_bytes + q * b_sub);
+                        if constexpr (PAIR) {
+                            // 3-D maps: one box brings the stage's kbs K-blocks (one TMA operation
+                            // each for A and B, as many as a 256-row box takes in one CTA)
+                            if (q == 0) {
+                                tma_load_3d_pair(a_dst, &map_a, fb, 0, tile0 * BM, ks * kbs);
+                                tma_load_3d_pair_policy(b_dst, wide, fb, 0, b_row, ks * kbs, stream_policy);
+                            }
+                            continue;
+                        }
+                        tma_load_2d(a_dst, &map_a, full_bar(stage), x, tile0 * BM);
                         // the weights stream through once: evict-first in L2 (measured on GB300:
                         // 197.3 vs 198.0 us at 16 rows, 248.3 vs 250.0 at 64, 449.9 vs 455.1 at 512)
                         if (ch.n == args.bn || MT == 2) {
@@ -310,14 +350,21 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                 }
             }
             if (!ok) {
-                // let the copies already issued land before the CTA leaves
-                const long long first = issued > stages ? issued - stages : 0;
-                for (long long n = first; n < issued; ++n)
-                    drain_wait(full_bar(static_cast<int>(n % stages)), static_cast<uint32_t>((n / stages) & 1));
+                // let the copies already issued land before the CTA leaves (a pair's second CTA
+                // cannot wait on the issuer's barriers: it gives them a fixed 100 us)
+                if (PAIR && !issuer) {
+                    const unsigned long long t0 = globaltimer_ns();
+                    while (globaltimer_ns() - t0 < 100000ull) {
+                    }
+                } else {
+                    const long long first = issued > stages ? issued - stages : 0;
+                    for (long long n = first; n < issued; ++n)
+                        drain_wait(full_bar(static_cast<int>(n % stages)), static_cast<uint32_t>((n / stages) & 1));
+                }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && (!PAIR || issuer)) {
             // ---------------- MMA issuer
             int stage = 0;
             uint32_t phase = 0;
@@ -326,7 +373,7 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                 const int buf = c % n_bufs;
                 const uint32_t use = static_cast<uint32_t>(c / n_bufs);
                 const Chunk ch = chunk_of(args, slice, c);
-                const uint32_t idesc = idesc_bf16_f32(BM, ch.n);
+                const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * BM : BM, ch.n);
                 if (!mbar_wait(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag)) {
                     ok = false;
                     break;
@@ -346,23 +393,39 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                             const uint32_t a0 = st + static_cast<uint32_t>((q * mt + t) * args.a_bytes);
                             const uint32_t d = d_tmem + static_cast<uint32_t>(t * args.bn);
 #pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk)
-                                umma_bf16(d, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(b0 + kk * 32), idesc,
-                                          (ks | q | kk) != 0 ? 1u : 0u);
+                            for (int kk = 0; kk < BK / 16; ++kk) {
+                                const uint64_t ad = sw128_kmajor_desc(a0 + kk * 32);
+                                const uint64_t bd = sw128_kmajor_desc(b0 + kk * 32);
+                                const uint32_t acc = (ks | q | kk) != 0 ? 1u : 0u;
+                                if constexpr (PAIR)
+                                    umma_bf16_pair(d, ad, bd, idesc, acc);
+                                else
+                                    umma_bf16(d, ad, bd, idesc, acc);
+                            }
                         }
                     }
-                    umma_commit(empty_bar(stage));
+                    if constexpr (PAIR)
+                        umma_commit_pair_both(empty_bar(stage));  // both CTAs' producers reuse the stage
+                    else
+                        umma_commit(empty_bar(stage));
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok)
-                    umma_commit(tfull_bar(buf));
+                if (ok) {
+                    if constexpr (PAIR)
+                        umma_commit_pair_both(tfull_bar(buf));
+                    else
+                        umma_commit(tfull_bar(buf));
+                }
             }
             if (!ok) {
                 // every MMA issued so far must finish before TMEM is released
-                umma_commit(drain_bar);
+                if constexpr (PAIR)
+                    umma_commit_pair(drain_bar);
+                else
+                    umma_commit(drain_bar);
                 drain_wait(drain_bar, 0);
             }
         }
@@ -470,7 +533,10 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
                 }
             }
             tc_fence_before();
-            mbar_arrive(tempty_bar(buf));
+            if (PAIR && !issuer)
+                mbar_arrive_cluster(mapa_shared(tempty_bar(buf), 0u));
+            else
+                mbar_arrive(tempty_bar(buf));
             drain_queue();  // overlaps the next chunk's MMAs
             if (slots && !ch.store && top.v[0] > published) {
                 atomicMax(slots + split % KP, order_key(top.v[0]));
@@ -491,10 +557,15 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR)
+        cluster_sync();  // neither CTA leaves while the other may still signal or read it
     tc_fence_after();
     if (warp == 1) {
         __syncwarp();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, TMEM_COLS);
     }
     if (threadIdx.x == 0 && *abort_flag)
         atomicOr(args.status, kStatusTimeoutGemm);
@@ -546,13 +617,32 @@ cudaError_t encode_map(CUtensorMap *map, const void *ptr, int K, int rows, int b
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The same matrix as a 3-D view (x = 64 elements of K, y = row, z = K-block; K a multiple of
+// 64): a box of 64 x box_rows x kb lands as kb consecutive 128-byte-swizzled K-major tiles.
+cudaError_t encode_map3(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows, int kb)
+{
+    auto encode = tensor_map_encoder();
+    if (!encode || K % BK != 0)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(BK), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(K / BK)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(BK) * 2};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_rows),
+                               static_cast<cuuint32_t>(kb)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+                              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // A map is a pure function of its encode parameters, so a drafting loop that calls with the
 // same buffers every step reuses the encodings (a small per-thread cache, oldest entry out).
-cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows)
+cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows, int kb = 0)
 {
     struct Entry {
         const void *ptr;
-        int K, rows, box_rows;
+        int K, rows, box_rows, kb;  // kb = 0: the 2-D map
         CUtensorMap map;
     };
     constexpr int kEntries = 16;
@@ -560,18 +650,23 @@ cudaError_t make_map(CUtensorMap *map, const void *ptr, int K, int rows, int box
     thread_local int used = 0, next = 0;
     for (int i = 0; i < used; ++i) {
         const Entry &e = cache[i];
-        if (e.ptr == ptr && e.K == K && e.rows == rows && e.box_rows == box_rows) {
+        if (e.ptr == ptr && e.K == K && e.rows == rows && e.box_rows == box_rows && e.kb == kb) {
             *map = e.map;
             return cudaSuccess;
         }
     }
-    const cudaError_t err = encode_map(map, ptr, K, rows, box_rows);
+    const cudaError_t err = kb ? encode_map3(map, ptr, K, rows, box_rows, kb) : encode_map(map, ptr, K, rows, box_rows);
     if (err != cudaSuccess)
         return err;
-    cache[next] = Entry{ptr, K, rows, box_rows, *map};
+    cache[next] = Entry{ptr, K, rows, box_rows, kb, *map};
     next = (next + 1) % kEntries;
     used = used < kEntries ? used + 1 : kEntries;
     return cudaSuccess;
+}
+
+cudaError_t make_map3(CUtensorMap *map, const void *ptr, int K, int rows, int box_rows, int kb)
+{
+    return make_map(map, ptr, K, rows, box_rows, kb);
 }
 
 template <int KP>
@@ -589,13 +684,24 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     args.bn = R <= 64 ? 128 : BN;
     args.kbs = R <= 64 ? 2 : 1;
     args.row_tiles = (R + BM - 1) / BM;
-    // Beyond 128 rows a CTA takes two row tiles against each chunk of B; their 256-column
-    // accumulators fill TMEM, so the chunk's accumulator is single-buffered.
-    args.mt = args.bn == BN && args.row_tiles >= 2 ? 2 : 1;
+    // Beyond 128 rows two row tiles share each chunk of B.  As a CTA pair each SM holds one
+    // tile and half of B, so an accumulator takes 256 TMEM columns and the epilogue runs under
+    // the next chunk's MMAs (two buffers); in one CTA (mt = 2) the two tiles' accumulators
+    // fill TMEM (one buffer) and the MMA waits for the epilogue.  Both take 64 KB of operands
+    // per stage in two TMA operations (three stages).  Measured on GB300 (same bits): pairs
+    // 464.4 -> 429.6 us per call at 512 rows; at 1024 rows, where the kernel runs long enough
+    // to settle at the power cap, 1760.1 -> 1772.7 us, so larger row counts stay in one CTA.
+    const bool two_tiles = args.bn == BN && args.row_tiles >= 2;
+    // pairs read A and B through 3-D views whose K-blocks must not straddle rows
+    args.pair = two_tiles && args.row_tiles <= 4 && K % BK == 0 ? 1 : 0;
+    if (args.pair)
+        args.kbs = 2;
+    args.mt = two_tiles && !args.pair ? 2 : 1;
     args.n_bufs = 2 * args.mt * args.bn <= TMEM_COLS ? 2 : 1;
-    args.row_groups = (args.row_tiles + args.mt - 1) / args.mt;
+    args.row_groups = args.pair ? (args.row_tiles + 1) / 2 * 2 : (args.row_tiles + args.mt - 1) / args.mt;
+    const int b_box = args.pair ? args.bn / 2 : args.bn;  // rows of the wide B box
     const int stash_bytes = args.mt * STASH_TILE_BYTES;
-    const int stage_bytes = args.kbs * (args.mt * args.a_bytes + args.bn * BK * 2);
+    const int stage_bytes = args.kbs * (args.mt * args.a_bytes + b_box * BK * 2);
     args.stages = std::min(MAX_STAGES, (SMEM_LIMIT - 1024 - BAR_BYTES - stash_bytes) / stage_bytes);
     if (args.stages < 2 || args.a_bytes + args.bn * BK * 2 < A_TILE_BYTES)
         return cudaErrorInvalidConfiguration;
@@ -604,18 +710,23 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     CUtensorMap ma, mtw, mtn, msw, msn;
     cudaError_t e;
     // two row tiles per CTA: one box covers both (256 rows, the largest TMA box)
-    if ((e = make_map(&ma, A, K, R, args.mt == 2 ? 2 * a_rows : a_rows)) != cudaSuccess)
+    const int a_box = args.mt == 2 ? 2 * a_rows : a_rows;
+    if ((e = args.pair ? make_map3(&ma, A, K, R, a_box, args.kbs) : make_map(&ma, A, K, R, a_box)) != cudaSuccess)
         return e;
     // an empty segment gets the other segment's maps (never read)
     const void *tb = n_topk > 0 ? Bt : Bs;
     const int tn = n_topk > 0 ? n_topk : n_store;
     const void *sb = n_store > 0 ? Bs : Bt;
     const int sn = n_store > 0 ? n_store : n_topk;
-    if ((e = make_map(&mtw, tb, K, tn, args.bn)) != cudaSuccess ||
+    if ((e = args.pair ? make_map3(&mtw, tb, K, tn, b_box, args.kbs) : make_map(&mtw, tb, K, tn, b_box)) !=
+            cudaSuccess ||
         (e = make_map(&mtn, tb, K, tn, UNIT)) != cudaSuccess ||
-        (e = make_map(&msw, sb, K, sn, args.bn)) != cudaSuccess || (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
+        (e = args.pair ? make_map3(&msw, sb, K, sn, b_box, args.kbs) : make_map(&msw, sb, K, sn, b_box)) !=
+            cudaSuccess ||
+        (e = make_map(&msn, sb, K, sn, UNIT)) != cudaSuccess)
         return e;
-    auto kern = args.mt == 1 ? gemm_tc_kernel<KP, 1> : gemm_tc_kernel<KP, 2>;
+    auto kern = args.pair ? gemm_tc_kernel<KP, 1, true>
+                          : (args.mt == 1 ? gemm_tc_kernel<KP, 1, false> : gemm_tc_kernel<KP, 2, false>);
     if ((e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), smem_bytes)) != cudaSuccess)
         return e;
     const int sms = device_sm_count();
@@ -629,18 +740,45 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     // time (one tile per CTA; measured on GB300: 205.6 -> 201.1 us per back-to-back call at
     // 16 rows); with two tiles the feed is bound by TMA operations and the prefetch costs
     // (1739 -> 1797 us at 1024 rows), so those launches stay plain.
-    if (args.mt != 1)
+    if (args.mt != 1 || args.pair)
         args.dependent = 0;
-    // the shared bound pays where the MMA waits for the epilogue (one accumulator buffer)
+    // the shared bound pays where the MMA waits for the epilogue (one accumulator buffer; with
+    // pairs, measured on GB300, it cost 7 us at 512 rows)
     if (args.n_bufs != 1 || n_topk == 0) {
         args.bound = nullptr;
         args.group_done = nullptr;
     }
-    args.n_split = std::max(1, std::min({max_splits_for(R), units, std::max(1, sms / args.row_groups)}));
+    int ctas = sms;  // CTAs resident at once: one per SM
+    if (args.pair) {
+        // pairs need two SMs of one GPC: size the grid by the pairs that fit at once
+        static int pair_ctas[4] = {0, 0, 0, 0};  // per KP instantiation
+        int &cached = pair_ctas[KP == 4 ? 0 : KP == 8 ? 1 : KP == 16 ? 2 : 3];
+        if (cached == 0) {
+            cudaLaunchConfig_t qc = {};
+            qc.gridDim = dim3(static_cast<unsigned>(2 * sms));
+            qc.blockDim = dim3(64 + BM);
+            qc.dynamicSmemBytes = smem_bytes;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 2;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            qc.attrs = qa;
+            qc.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &qc) != cudaSuccess || clusters < 1) {
+                (void)cudaGetLastError();
+                clusters = sms / 2;
+            }
+            cached = std::min(sms, 2 * clusters);
+        }
+        ctas = cached;
+    }
+    args.n_split = std::max(1, std::min({max_splits_for(R), units, std::max(1, ctas / args.row_groups)}));
     if (n_split_out)
         *n_split_out = args.n_split;
     const dim3 grid(static_cast<unsigned>(args.row_groups * args.n_split));
-    if (!args.dependent) {
+    if (!args.dependent && !args.pair) {
         kern<<<grid, 64 + args.mt * BM, smem_bytes, stream>>>(ma, mtw, mtn, msw, msn, args);
         return cudaGetLastError();
     }
@@ -650,8 +788,16 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (args.pair) {
+        // CTAs 2i and 2i + 1 (row tiles 2j and 2j + 1 of one slice: row_groups is even)
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+    } else {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+    }
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if ((e = cudaLaunchKernelEx(&cfg, kern, ma, mtw, mtn, msw, msn, args)) != cudaSuccess)

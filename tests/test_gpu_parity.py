@@ -689,7 +689,22 @@ def _random_multi_tile_shapes(n, seed):
     return out
 
 
-@pytest.mark.parametrize("B,T,H,V,k,D", _random_shapes(24, 2024) + _random_multi_tile_shapes(8, 2025))
+def _random_pair_shapes(n, seed):
+    """129 to 512 rows with H a multiple of 64: the LM head as CTA pairs (one 128-row tile per
+    CTA, M = 256 per pair), odd tile counts (a pair whose second tile is empty), ragged last
+    tiles, narrow last chunks of a slice and of the gate segment, KP up to 32."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        k = 32 if i == 0 else int(rng.integers(1, 33))
+        T = int(rng.integers(1, 18))
+        B = int(rng.integers(-(-129 // T), 512 // T + 1))
+        out.append((B, T, 64 * int(rng.integers(1, 41)), int(rng.integers(k, 9001)), k, 8 * int(rng.integers(1, 41))))
+    return out
+
+
+@pytest.mark.parametrize("B,T,H,V,k,D", _random_shapes(24, 2024) + _random_multi_tile_shapes(8, 2025) +
+                         _random_pair_shapes(8, 2026))
 def test_select_random_shapes(B, T, H, V, k, D):
     """Seeded random shapes across the limits: the fused path against the oracle under the same rules."""
     cfg, x = small_case(B, T, H, V, k, D, seed=B * 1000 + T * 10 + k)
