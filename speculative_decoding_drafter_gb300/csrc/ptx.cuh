@@ -254,27 +254,10 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
-// tma_load_2d into this CTA's shared memory, completing on an mbarrier of either CTA of the
-// pair (`bar` a shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y)
-{
-    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_pair_policy(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
-                                                        int y, uint64_t policy)
-{
-    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-                 ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
-                 : "memory");
-}
-
-// A box of a 3-D view (x = 64 elements of K, y = row, z = K-block): `z` boxes of 64 x rows
-// land as consecutive 128-byte-swizzled K-major tiles, one per K-block.
+// A box of a 3-D view (x = 64 elements of K, y = row, z = K-block) into this CTA's shared
+// memory, completing on an mbarrier of either CTA of the pair (`bar` a shared::cluster
+// address): a box of 64 x rows x kb lands as kb consecutive 128-byte-swizzled K-major tiles,
+// one per K-block.
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
                                                  int z)
 {

@@ -153,31 +153,197 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
     }
 }
 
-// One warp per row: merge n_split sorted lists of KP into the row's top-k.
+// Few rows (a grid of one wave): one CTA per (row, 4096-column slice), a
+// thread holding 16 values in registers.  The per-warp list of the kernel above spends most of
+// its time in the chain of insertions while a list fills, which at 16 rows is the whole
+// kernel; here no list is filled value by value.  Warp w takes tau_w, the ceil(KP / 8)-th
+// largest of its lanes' maxima: at least ceil(KP / 8) values of distinct columns are at or
+// above it, so over the 8 warps at least KP values are at or above tau = min_w tau_w, which
+// therefore bounds the slice's KP-th best from below.  The values at or above tau (typically
+// a few dozen) are gathered in shared memory and warp 0 sorts them 32 at a time into the
+// slice's top-KP.  The gather holds every value of the slice, so no count can overflow it.
+constexpr int kSmallPerThread = 16;                          // values per thread
+constexpr int kSmallCols = kThreads * kSmallPerThread;       // columns per CTA
+
+template <int KP>
+__global__ void __launch_bounds__(kThreads) logits_topk_small_kernel(const float *__restrict__ logits, int V,
+                                                                     int n_split, float *__restrict__ pval,
+                                                                     int32_t *__restrict__ pid)
+{
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();  // launched as a programmatic dependent
+    __shared__ float s_v[kSmallCols];
+    __shared__ int s_i[kSmallCols];
+    __shared__ float s_tau[kWarps];
+    __shared__ int s_count;
+    const int r = blockIdx.x;
+    const int s = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int c0 = s * kSmallCols;           // first column of the slice (V is a multiple of 4)
+    const int c1 = min(V, c0 + kSmallCols);
+    const float4 *row4 = reinterpret_cast<const float4 *>(logits + static_cast<long long>(r) * V);
+    if (threadIdx.x == 0)
+        s_count = 0;
+    // group q of this thread: columns 4 * g .. 4 * g + 3, g = c0 / 4 + q * kThreads + tid
+    float x[kSmallPerThread];
+#pragma unroll
+    for (int q = 0; q < kSmallPerThread / 4; ++q) {
+        const int g = c0 / 4 + q * kThreads + threadIdx.x;
+        const float4 v = 4 * g < c1 ? __ldcs(row4 + g) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        x[4 * q] = v.x;
+        x[4 * q + 1] = v.y;
+        x[4 * q + 2] = v.z;
+        x[4 * q + 3] = v.w;
+    }
+    bool any = false;  // this thread holds a column of the slice
+    float m = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kSmallPerThread / 4; ++q) {
+        const int g = c0 / 4 + q * kThreads + threadIdx.x;
+        if (4 * g < c1) {
+            any = true;
+            m = fmaxf(m, fmaxf(fmaxf(x[4 * q], x[4 * q + 1]), fmaxf(x[4 * q + 2], x[4 * q + 3])));
+        }
+    }
+    // tau_w: the ceil(KP / 8)-th largest lane maximum of the warp (-inf when fewer lanes hold
+    // columns, which makes every value of the slice a survivor)
+    float mv = any ? m : -INFINITY;
+    int mi = any ? lane : INT_MAX;
+    warp_sort_desc(mv, mi);
+    constexpr int kJ = (KP + kWarps - 1) / kWarps;
+    const float tw = __shfl_sync(kFullMask, mv, kJ - 1);
+    const int tiw = __shfl_sync(kFullMask, mi, kJ - 1);
+    if (lane == 0)
+        s_tau[warp] = tiw == INT_MAX ? -INFINITY : tw;
+    __syncthreads();
+    float tau = s_tau[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w)
+        tau = fminf(tau, s_tau[w]);
+    // gather the survivors: values at or above tau of columns inside the slice
+#pragma unroll
+    for (int q = 0; q < kSmallPerThread / 4; ++q) {
+        const int g = c0 / 4 + q * kThreads + threadIdx.x;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (4 * g + c < c1 && x[4 * q + c] >= tau) {
+                const int slot = atomicAdd(&s_count, 1);
+                s_v[slot] = x[4 * q + c];
+                s_i[slot] = 4 * g + c;
+            }
+        }
+    }
+    __syncthreads();
+    if (warp != 0)
+        return;
+    // warp 0: the top 32 of the survivors, 32 at a time (each batch sorted, then merged into
+    // the running list with one bitonic clean); lane j ends with the j-th best
+    const int count = s_count;
+    float bv = -INFINITY;
+    int bi = INT_MAX;
+    for (int b0 = 0; b0 < count; b0 += 32) {
+        float v = b0 + lane < count ? s_v[b0 + lane] : -INFINITY;
+        int i = b0 + lane < count ? s_i[b0 + lane] : INT_MAX;
+        warp_sort_desc(v, i);
+        if (b0 == 0) {
+            bv = v;
+            bi = i;
+            continue;
+        }
+        // best (descending) against the batch reversed: the better of each pair holds the top
+        // 32 of both as a bitonic sequence
+        const float rv = __shfl_sync(kFullMask, v, 31 - lane);
+        const int ri = __shfl_sync(kFullMask, i, 31 - lane);
+        if (ranks_before(rv, ri, bv, bi)) {
+            bv = rv;
+            bi = ri;
+        }
+#pragma unroll
+        for (int stride = 16; stride > 0; stride >>= 1) {
+            const float ov = __shfl_xor_sync(kFullMask, bv, stride);
+            const int oi = __shfl_xor_sync(kFullMask, bi, stride);
+            const bool lower = (lane & stride) == 0;
+            if (lower == ranks_before(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+    }
+    if (lane < KP) {
+        const long long o = (static_cast<long long>(r) * n_split + s) * KP + lane;
+        pval[o] = bv;
+        pid[o] = bi;
+    }
+}
+
+// One warp per row: merge n_split sorted lists of KP into the row's top-k.  Lane l merges
+// whole lists l, l + 32, ... into its own sorted top-KP; the lanes' lists are then combined
+// by gathering the entries at or above a bound on the row's KP-th best (bounded_merge), or,
+// when more than 32 are, by the warp butterfly.  (Offering every entry to one warp-wide list
+// cost 12.7 us at 16 rows x 38 lists of 8 and 30.5 us at 16 x 64 lists of 16, measured on
+// GB300: each insertion is a chain of dependent shuffles.)
+template <int KP>
 __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float *__restrict__ pval,
-                                                              const int32_t *__restrict__ pid, int R, int total,
+                                                              const int32_t *__restrict__ pid, int R, int n_split,
                                                               int k, int32_t *__restrict__ ids,
                                                               float *__restrict__ vals)
 {
     if (threadIdx.x == 0)
         griddep_launch_dependents();
     griddep_wait();  // launched as a programmatic dependent
-    const int r = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    __shared__ float s_mv[kWarps][32];
+    __shared__ int s_mi[kWarps][32];
+    const int warp = threadIdx.x >> 5;
+    const int r = blockIdx.x * kWarps + warp;
     const int lane = threadIdx.x & 31;
     if (r >= R)
         return;
-    const long long base = static_cast<long long>(r) * total;
-    WarpList wl;
-    wl.init();
-    for (int c = 0; c < total; c += 32) {
-        const int idx = c + lane;
-        const float cv = idx < total ? pval[base + idx] : -INFINITY;
-        const int ci = idx < total ? pid[base + idx] : INT_MAX;
-        wl.offer(cv, ci, k);
+    float av[KP];
+    int ai[KP];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+        av[j] = -INFINITY;
+        ai[j] = INT_MAX;
+    }
+    const long long row_base = static_cast<long long>(r) * n_split * KP;
+    for (int list = lane; list < n_split; list += 32) {
+        const float4 *pv = reinterpret_cast<const float4 *>(pval + row_base + static_cast<long long>(list) * KP);
+        const int4 *pi = reinterpret_cast<const int4 *>(pid + row_base + static_cast<long long>(list) * KP);
+        float bv[KP];
+        int bi[KP];
+#pragma unroll
+        for (int q = 0; q < KP / 4; ++q) {
+            const float4 v4 = __ldcg(pv + q);
+            const int4 i4 = __ldcg(pi + q);
+            bv[4 * q] = v4.x;
+            bv[4 * q + 1] = v4.y;
+            bv[4 * q + 2] = v4.z;
+            bv[4 * q + 3] = v4.w;
+            bi[4 * q] = i4.x;
+            bi[4 * q + 1] = i4.y;
+            bi[4 * q + 2] = i4.z;
+            bi[4 * q + 3] = i4.w;
+        }
+        merge_top<KP>(av, ai, bv, bi);
+    }
+    float mv;
+    int mi;
+    if (!(KP <= 16 && bounded_merge<KP>(av, ai, s_mv[warp], s_mi[warp], mv, mi))) {
+        warp_merge_top<KP>(av, ai, 31);  // every lane now holds the row's top-KP
+        mv = -INFINITY;
+        mi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < KP; ++j)
+            if (j == lane) {
+                mv = av[j];
+                mi = ai[j];
+            }
     }
     if (lane < k) {
-        ids[static_cast<long long>(r) * k + lane] = wl.i;
-        vals[static_cast<long long>(r) * k + lane] = wl.v;
+        ids[static_cast<long long>(r) * k + lane] = mi;
+        vals[static_cast<long long>(r) * k + lane] = mv;
     }
 }
 
@@ -189,12 +355,21 @@ cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32
     // warp pays a warm-up of ~k (1 + ln(n / k)) list insertions over its n values, so long slices
     // win once the CTAs cover the SMs (measured on GB300: 78 us at 512 rows x 151936 with one
     // slice per row, 95 us with two, 139 us with four).
+    const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
     const int sms = device_sm_count();
+    // Few rows: slices of 4096 columns without per-warp lists, while the grid fits one wave
+    // (measured on GB300, same ids and values: 28.3 -> 26.3 us per call at 16 x 151936, 40.6 ->
+    // 35.6 at 16 x 262144; 32.4 -> 38.6 at 64 x 152064, 2432 CTAs, so larger grids keep the lists)
+    const int small_split = (V + kSmallCols - 1) / kSmallCols;
+    if (vec4 && static_cast<long long>(R) * small_split <= 8ll * sms && small_split <= max_splits_for(R)) {
+        *n_split_out = small_split;
+        return launch_dependent(logits_topk_small_kernel<KP>, dim3(static_cast<unsigned>(R), small_split),
+                                dim3(kThreads), 0, stream, logits, V, small_split, pval, pid);
+    }
     int n_split = std::max(1, (sms + R - 1) / R);
     n_split = std::min({n_split, max_splits_for(R), std::max(1, V / 2048)});
     *n_split_out = n_split;
     const dim3 grid(static_cast<unsigned>(R), static_cast<unsigned>(n_split));
-    const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
     if (vec4)
         return launch_dependent(logits_topk_partial_kernel<KP, true>, grid, dim3(kThreads), 0, stream, logits, V,
                                 n_split, pval, pid);
@@ -220,8 +395,22 @@ cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int 
                               int32_t *topk_ids, float *topk_vals, cudaStream_t stream)
 {
     const dim3 grid(static_cast<unsigned>((R + kWarps - 1) / kWarps));
-    return launch_dependent(topk_merge_kernel, grid, dim3(kThreads), 0, stream, pval, pid, R, n_split * KP, k,
-                            topk_ids, topk_vals);
+    switch (KP) {
+    case 4:
+        return launch_dependent(topk_merge_kernel<4>, grid, dim3(kThreads), 0, stream, pval, pid, R, n_split, k,
+                                topk_ids, topk_vals);
+    case 8:
+        return launch_dependent(topk_merge_kernel<8>, grid, dim3(kThreads), 0, stream, pval, pid, R, n_split, k,
+                                topk_ids, topk_vals);
+    case 16:
+        return launch_dependent(topk_merge_kernel<16>, grid, dim3(kThreads), 0, stream, pval, pid, R, n_split, k,
+                                topk_ids, topk_vals);
+    case 32:
+        return launch_dependent(topk_merge_kernel<32>, grid, dim3(kThreads), 0, stream, pval, pid, R, n_split, k,
+                                topk_ids, topk_vals);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace df2

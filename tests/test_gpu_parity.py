@@ -307,6 +307,25 @@ def test_topk_stage_is_exact(R, V, k):
     assert np.array_equal(host(vals).view(np.uint32), o_vals.view(np.uint32))
 
 
+@pytest.mark.parametrize("R,V,k,kind", [(4, 8192, 16, "constant"), (3, 12300, 32, "two_levels"), (2, 4096, 4, "constant"),
+                                        (5, 20000, 8, "coarse")])
+def test_topk_stage_ties_in_small_slices(R, V, k, kind):
+    """Few rows run the 4096-column slice kernel: with every value of a slice tied at the bound all
+    of them are gathered (up to the whole slice) and sorted 32 at a time; the lower id must win."""
+    rng = np.random.default_rng(R * V + k)
+    if kind == "constant":
+        lg = np.full((R, V), 1.5, np.float32)
+    elif kind == "two_levels":
+        lg = np.where(rng.random((R, V)) < 0.3, np.float32(2.0), np.float32(-1.0)).astype(np.float32)
+    else:  # few distinct values: long runs of ties everywhere
+        lg = (rng.integers(0, 5, size=(R, V)) * 0.25).astype(np.float32)
+    lg[0, V - 1] = 3.0  # a single maximum in the last column of the last slice
+    ids, vals = df.dflash2_topk(dev(lg), k)
+    o_ids, o_vals = oracle.topk(lg, k)
+    assert np.array_equal(host(ids), o_ids)
+    assert np.array_equal(host(vals).view(np.uint32), o_vals.view(np.uint32))
+
+
 @pytest.mark.parametrize("R,H,D", [(8, 256, 64), (33, 200, 24), (300, 4096, 256), (1024, 512, 512)])
 def test_gate_stage(R, H, D):
     rng = np.random.default_rng(R + H + D)
