@@ -300,6 +300,16 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float *__res
     const int lane = threadIdx.x & 31;
     if (r >= R)
         return;
+    if (n_split == 1) {
+        // one slice covered the whole row: its sorted list is the row's top-KP (the lane
+        // butterfly below would merge it with 31 lanes of empty entries)
+        if (lane < k) {
+            const long long o = static_cast<long long>(r) * KP + lane;
+            ids[static_cast<long long>(r) * k + lane] = __ldcg(pid + o);
+            vals[static_cast<long long>(r) * k + lane] = __ldcg(pval + o);
+        }
+        return;
+    }
     float av[KP];
     int ai[KP];
 #pragma unroll

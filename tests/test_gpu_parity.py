@@ -292,7 +292,8 @@ def test_lm_head_logits_stage(R, H, V):
     assert np.all(np.abs(got.astype(np.float64) - ora) <= bound + 1e-30)
 
 
-@pytest.mark.parametrize("R,V,k", [(3, 50, 5), (16, 151936, 8), (7, 4099, 32), (2, 40, 32), (5, 3000, 1), (64, 262144, 16)])
+@pytest.mark.parametrize("R,V,k", [(3, 50, 5), (16, 151936, 8), (7, 4099, 32), (2, 40, 32), (5, 3000, 1), (64, 262144, 16),
+                                   (300, 20000, 16), (160, 8, 5)])
 def test_topk_stage_is_exact(R, V, k):
     rng = np.random.default_rng(V + k)
     lg = rng.standard_normal((R, V)).astype(np.float32)
