@@ -190,9 +190,11 @@ DF2_API df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32
  * Same kernels and results as dflash2_topk; the per-slice partial lists live in an
  * 8 MiB array inside the library's device image (held by every GPU that loads the
  * library until exit), so B*T*KP must not exceed 4096 (KP = k rounded up to 4, 8, 16 or
- * 32); larger requests return DF2_ERR_UNSUPPORTED.  The first call on a device looks up
- * that array's device address (cudaGetSymbolAddress) with the device current; make that
- * first call before any stream capture.  All calls share the array: calls that overlap on
+ * 32); larger requests return DF2_ERR_UNSUPPORTED.  The first call on a device (per CUDA
+ * context) looks up that array's device address (cudaGetSymbolAddress) with the device
+ * current; make that first call before any stream capture.  The address is kept for the
+ * life of the context: do not call across a device reset (cudaDeviceReset), which may
+ * bring the context back under the same handle.  All calls share the array: calls that overlap on
  * the GPU (other streams, other host threads) race and must be serialised by the caller.
  * Every entry the kernels read is written earlier in the same call, so nothing needs
  * clearing.  The method pages have no counterpart: this is a deployment variant. */

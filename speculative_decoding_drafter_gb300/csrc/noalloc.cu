@@ -7,6 +7,7 @@
 // where cudaMalloc's implicit device synchronisation is not acceptable.  This variant
 // keeps those partial lists in a fixed array that lives in the library's own device
 // image, so a call needs only its inputs and outputs.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -23,10 +24,38 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_topk_scratch[kNoAllocScratchBytes];
 
-// Device address of g_topk_scratch, looked up once per device with that device current.
-// (In host code the symbol name is only a host-side stand-in, never a device address.)
+// Device address of g_topk_scratch, looked up once per device and CUDA context, with that
+// device current.  (In host code the symbol name is only a host-side stand-in, never a
+// device address.)  Keying by the context as well as the device keeps a caller that switches
+// contexts on one device from getting another context's address.  A device reset
+// (cudaDeviceReset) may recreate the primary context under the same handle, so the library
+// must not be used across a reset.
 std::mutex g_mu;
-void *g_scratch_ptr[64] = {nullptr};
+struct ScratchEntry {
+    int dev;
+    CUcontext ctx;
+    void *ptr;
+};
+constexpr int kScratchEntries = 64;
+ScratchEntry g_scratch[kScratchEntries];
+int g_scratch_used = 0;
+
+CUcontext current_context()
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    static GetCurrent fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<GetCurrent>(p);
+    }
+    CUcontext ctx = nullptr;
+    if (!fn || fn(&ctx) != CUDA_SUCCESS)
+        return nullptr;
+    return ctx;
+}
 
 cudaError_t scratch_for_current_device(void **out)
 {
@@ -34,17 +63,26 @@ cudaError_t scratch_for_current_device(void **out)
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
-    if (dev < 0 || dev >= 64)
-        return cudaErrorInvalidDevice;
+    // (null before the first runtime call on this thread: the lookup below then makes the
+    // device's primary context current, and the context is read again)
+    CUcontext ctx = current_context();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_topk_scratch);
-        if (e != cudaSuccess)
-            return e;
-        g_scratch_ptr[dev] = p;
+    for (int i = 0; i < g_scratch_used; ++i)
+        if (g_scratch[i].dev == dev && g_scratch[i].ctx == ctx && ctx != nullptr) {
+            *out = g_scratch[i].ptr;
+            return cudaSuccess;
+        }
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_topk_scratch);
+    if (e != cudaSuccess)
+        return e;
+    if (ctx == nullptr)
+        ctx = current_context();
+    if (ctx != nullptr) {
+        const int slot = g_scratch_used < kScratchEntries ? g_scratch_used++ : (dev % kScratchEntries);
+        g_scratch[slot] = ScratchEntry{dev, ctx, p};
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

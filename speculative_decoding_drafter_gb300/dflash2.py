@@ -130,6 +130,11 @@ def _ptr(t, dtype, shape, name):
         return None
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if t.get_device() != torch.cuda.current_device():
+        # the library launches on the current device (and takes that device's scratch): a
+        # tensor on another device would be read across devices
+        raise ValueError(f"{name} is on cuda:{t.get_device()}, not on the current device "
+                         f"cuda:{torch.cuda.current_device()} (use torch.cuda.device(...))")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
