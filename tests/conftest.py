@@ -27,3 +27,16 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Prints the per-config counts of the full-size oracle comparisons (rows compared,
+    near-tie steps) that the GPU parity tests collected."""
+    try:
+        import parity_rules
+    except ImportError:  # pragma: no cover
+        return
+    if parity_rules.REPORT:
+        terminalreporter.section("full-size comparison with the oracle")
+        for line in parity_rules.REPORT:
+            terminalreporter.write_line(line)

@@ -57,10 +57,15 @@ def check_fused_candidates(gpu_ids, gpu_vals, ora_logits, ora_ids, ora_vals, tol
     return swaps
 
 
-def compare_lattice_and_draft(gpu_lat, gpu_draft, ora, T, k, tol, margin_floor=None):
+def compare_lattice_and_draft(gpu_lat, gpu_draft, ora, T, k, tol, margin_floor=None, stats=None):
     """Lattice scores where candidates agree; draft along each sequence while comparable.
 
-    Returns (compared_steps, low_margin_steps)."""
+    A step whose oracle walk margin is at or below the floor (a near tie that float32
+    rounding may decide either way) is counted as low-margin: if both sides still chose the
+    same candidate the sequence goes on (the next row reads the same predecessor row),
+    otherwise the paths part there and the rest of the sequence is not comparable.
+    Returns (compared_steps, low_margin_steps); `stats` (a dict) also receives
+    'agreed_low', 'parted' and 'unreached' counts."""
     B = gpu_draft.shape[0]
     R = B * T
     gpu_ids = gpu_lat[:, :k].astype(np.int64)
@@ -77,16 +82,32 @@ def compare_lattice_and_draft(gpu_lat, gpu_draft, ora, T, k, tol, margin_floor=N
             assert err <= tol[r], f"row {r}: lattice error {err} > {tol[r]}"
         if t == 0:
             assert np.all(gs[r] == gs[r][0:1]), f"row {r}: position-0 predecessor rows differ"
-    compared, low = 0, 0
+    compared, low, agreed_low, parted, unreached = 0, 0, 0, 0, 0
     floor = tol if margin_floor is None else margin_floor
     for b in range(B):
         for t in range(T):
             r = b * T + t
             if not same[r] or (t > 0 and not same[r - 1]):
+                unreached += T - t
                 break
             if ora["margins"][b, t] <= floor[r]:
                 low += 1
+                if gpu_draft[b, t] == ora["draft"][b, t]:
+                    agreed_low += 1
+                    continue
+                parted += 1
+                unreached += T - t - 1
                 break
             assert gpu_draft[b, t] == ora["draft"][b, t], f"sequence {b} position {t}: draft differs"
             compared += 1
+    if stats is not None:
+        stats.update(compared=compared, low=low, agreed_low=agreed_low, parted=parted, unreached=unreached)
     return compared, low
+
+
+# One line per full-size comparison, printed at the end of the pytest run (conftest).
+REPORT = []
+
+
+def report(line: str) -> None:
+    REPORT.append(line)
