@@ -80,4 +80,20 @@ def test_timing_rules_are_enforced(argv, monkeypatch):
 def test_defaults_finish_quickly_and_name_the_headline_workload(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.parse_args()
-    assert a.gpus == 1 and a.warmup >= 3 and a.config == "8b_b1" and a.impl == "ours" and a.op == "select"
+    # the largest single-GPU workload (1024 rows of a 262144-token vocabulary) is the headline
+    assert a.gpus == 1 and a.warmup >= 3 and a.config == "large_vocab" and a.impl == "ours" and a.op == "select"
+
+
+@pytest.mark.parametrize("steps,every,n", [(20, 2, 10), (10, 1, 10), (5, 1, 5), (1000, 8, 125), (80, 8, 10)])
+def test_enough_lm_head_launches_are_bracketed(steps, every, n):
+    assert bench.profile_every(steps) == every
+    assert len(range(0, steps, bench.profile_every(steps))) == n
+
+
+def test_both_arms_report_the_same_config():
+    for name in CONFIGS:
+        assert bench.bench_config(CONFIGS[name], 1) == bench.bench_config(CONFIGS[name], 1)
+    cfg = CONFIGS["large_vocab"]
+    c = bench.bench_config(cfg, 1)
+    assert c["workload"].startswith("large_vocab: B=64 T=16 H=5376 V=262144 k=16 D=512")
+    assert set(c) == {"workload", "l2", "parallelism"}
