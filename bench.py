@@ -585,9 +585,68 @@ def run_conv(args, rank: int, world: int):
 WALK_SHAPE = (8192, 16, 16)  # sequences, positions, candidates: a 143 MB lattice, larger than L2
 
 
+def fused_walk_cost(torch, df, cfg, steps: int, warmup: int):
+    """Step time of dflash2_select against dflash2_select_walk (p_min stop; and inverse-CDF sampling)
+    on one config: what moving the confidence walk into the selector call costs."""
+    _, d = select_inputs(torch, df, cfg)
+    B, T, k = cfg.B, cfg.T, cfg.k
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([0, 47])))
+    uni = torch.from_numpy(g.random((B, T), dtype=np.float32)).cuda()
+    n_draft = torch.empty((B,), dtype=torch.int32, device="cuda")
+    conf = torch.empty((B, T), dtype=torch.float32, device="cuda")
+    common = (d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"], d["anchor"], k, T)
+
+    def plain():
+        df.dflash2_select(*common, lattice=d["lattice"], draft_ids=d["draft"], workspace=d["ws"])
+
+    def pmin():
+        df.dflash2_select_walk(*common, temperature=1.0, p_min=0.3, lattice=d["lattice"], draft_ids=d["draft"],
+                               n_draft=n_draft, confidence=conf, workspace=d["ws"])
+
+    def sampled():
+        df.dflash2_select_walk(*common, temperature=1.0, p_min=0.3, uniforms=uni, lattice=d["lattice"],
+                               draft_ids=d["draft"], n_draft=n_draft, confidence=conf, workspace=d["ws"])
+
+    def separate():  # the plain call followed by the stand-alone sampling walk on its lattice
+        plain()
+        df.dflash2_walk_sample(d["lattice"], B, T, k, temperature=1.0, p_min=0.3, uniforms=uni, n_draft=n_draft,
+                               confidence=conf)
+
+    modes = {"select_us": plain, "select_walk_pmin_us": pmin, "select_walk_sampling_us": sampled,
+             "select_then_walk_sample_us": separate}
+    for f in modes.values():
+        for _ in range(warmup):
+            f()
+    torch.cuda.synchronize()
+    # blocks of a few back-to-back calls per mode, the modes interleaved block by block, so that a
+    # clock that drifts (a long tensor-bound run settles at the power cap) weighs on every mode alike
+    block = 5
+    rounds = max(1, steps // block)
+    ev = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(rounds)]
+          for m in modes}
+    for i in range(rounds):
+        for m, f in modes.items():
+            a, b = ev[m][i]
+            a.record()
+            for _ in range(block):
+                f()
+            b.record()
+    torch.cuda.synchronize()
+    out = {"workload": workload_name(cfg), "steps_per_mode": rounds * block,
+           "timing": f"{rounds} rounds of {block} back-to-back calls per mode, the modes interleaved"}
+    for m in modes:
+        out[m] = 1e3 * sum(a.elapsed_time(b) for a, b in ev[m]) / (rounds * block)
+    out["fused_sampling_walk_adds_us"] = out["select_walk_sampling_us"] - out["select_us"]
+    out["separate_sampling_walk_adds_us"] = out["select_then_walk_sample_us"] - out["select_us"]
+    del d
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_walk(args, rank: int, world: int):
     """The walk with confidence, p_min stop and inverse-CDF sampling (and the plain greedy walk) over a
-    seeded lattice of WALK_SHAPE.  One warp per sequence, T dependent row reads: latency-bound."""
+    seeded lattice of WALK_SHAPE.  One warp per sequence, T dependent row reads: latency-bound.  Also
+    the cost of the same walk inside the selector call (dflash2_select_walk) on --config."""
     import torch
 
     from speculative_decoding_drafter_gb300 import dflash2 as df
@@ -668,12 +727,13 @@ def run_walk(args, rank: int, world: int):
     g_draft, g_n = draft.cpu().numpy()[:sample_b], n_draft.cpu().numpy()[:sample_b]
     agree = float(np.mean(np.all(g_draft == o_draft, axis=1) & (g_n == o_n)))
     achieved = algo / (us / 1e6) / 1e9
+    fused = fused_walk_cost(torch, df, CONFIGS[args.config], max(args.steps, 50), args.warmup)
     print(json.dumps({
         "impl": "ours", "op": "walk", "metric": "sampling walk sequences/s", "value": B / (us / 1e6),
         "unit": "sequences/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": name, "l2": "flushed before every timed launch (256 MB write, outside the timing)"},
-        "greedy_walk_us": greedy_us, "sampling_walk_us": us,
+        "greedy_walk_us": greedy_us, "sampling_walk_us": us, "in_select_call": fused,
         "sample_agreement_with_oracle": agree, "agreement_sample": f"first {sample_b} sequences, exact draft and n_draft",
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None, "kernel": "walk_sample_kernel",

@@ -125,6 +125,33 @@ DF2_API df2_status dflash2_select(const df2_dims *dims, const void *hidden, cons
                           int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate,
                           void *workspace, size_t workspace_bytes, void *stream);
 
+/* Options of the walk at the end of dflash2_select_walk. */
+typedef struct df2_walk_opts {
+    float temperature;     /* > 0 and finite: p = softmax(S / temperature) on the row the walk reads */
+    float p_min;           /* the walk stops at the first position whose p is below it; <= 0 never stops */
+    const float *uniforms; /* [B, T] in [0, 1): inverse-CDF sampling; NULL: greedy (first maximum) */
+    int32_t *n_draft;      /* [B] tokens emitted per sequence, or NULL */
+    float *confidence;     /* [B, T] p of the chosen transition up to and including a stop, 0 after; or NULL */
+} df2_walk_opts;
+
+/*
+ * dflash2_select with the walk's confidence, the p_min early stop and sampling computed in
+ * the same launches: the last CTA of each sequence in the merge/lattice kernel walks the
+ * rows with the softmax of each row it reads, instead of the stored argmax ("DFlash2 Lands in
+ * llama.cpp", section "p_min Means Something Different Under DFlash2": the confidence is the
+ * softmax of the current transition row at the chosen candidate, and a low one stops the
+ * draft; "DFlash 2: Keep Drafting Parallel", section "A Lightweight Path Selector": sampling
+ * draws from the same scores).  The results are those of dflash2_walk_sample on the lattice
+ * this call writes, bit for bit: draft_ids is -1 from a stop on.  walk == NULL is
+ * dflash2_select.  The caller supplies the random numbers (uniforms), so a draw is
+ * reproducible.  Probabilities are float32 with expf.
+ */
+DF2_API df2_status dflash2_select_walk(const df2_dims *dims, const df2_walk_opts *walk, const void *hidden,
+                                       const void *W_vocab, const void *W_sel, const void *pred_cb,
+                                       const void *succ_cb, const int32_t *anchor, float *lattice,
+                                       int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate,
+                                       void *workspace, size_t workspace_bytes, void *stream);
+
 /*
  * Same path from given float32 logits [B*T, V] instead of the LM head: the top-k,
  * lattice and walk see exactly these logits (the unary score of a candidate is its
@@ -279,8 +306,8 @@ DF2_API df2_status dflash2_profile_events(void *begin, void *end);
 /* Static description of a status code. */
 DF2_API const char *dflash2_status_string(df2_status status);
 
-/* Library version as MAJOR*10000 + MINOR*100 + PATCH (0.2.0: the host-buffer select with
- * an optional page-locked status word, the bounded-wait self-test). */
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH (0.3.0: dflash2_select_walk, the
+ * confidence / p_min / sampling walk inside the selector call). */
 DF2_API int32_t dflash2_version(void);
 
 #ifdef __cplusplus

@@ -186,11 +186,12 @@ cudaError_t profile_mark(cudaEvent_t ev, cudaStream_t st) { return ev ? cudaEven
 // Shared tail of both select paths: merge, lattice and walk in one launch.
 df2_status finish(const df2_dims &d, const Workspace &w, int n_split, const float *gate, const void *pred_cb,
                   const void *succ_cb, const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
-                  float *topk_vals, cudaStream_t st, const HostMirrors &mirrors = HostMirrors{})
+                  float *topk_vals, cudaStream_t st, const HostMirrors &mirrors = HostMirrors{},
+                  const WalkOpts &walk = WalkOpts{})
 {
     DF2_CUDA(launch_finish(d.B, d.T, d.k, d.V, d.D, kp_for(d.k), n_split, w.pval, w.pid, gate,
                            static_cast<const uint16_t *>(pred_cb), static_cast<const uint16_t *>(succ_cb), anchor,
-                           lattice, draft_ids, topk_ids, topk_vals, w.best, w.counters, mirrors, st));
+                           lattice, draft_ids, topk_ids, topk_vals, w.best, w.counters, mirrors, walk, st));
     return DF2_OK;
 }
 
@@ -198,7 +199,8 @@ df2_status finish(const df2_dims &d, const Workspace &w, int n_split, const floa
 df2_status select_checked(const df2_dims &d, const void *hidden, const void *W_vocab, const void *W_sel,
                           const void *pred_cb, const void *succ_cb, const int32_t *anchor, float *lattice,
                           int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate, void *workspace,
-                          cudaStream_t st, const HostMirrors &mirrors = HostMirrors{})
+                          cudaStream_t st, const HostMirrors &mirrors = HostMirrors{},
+                          const WalkOpts &walk = WalkOpts{})
 {
     const Workspace w = carve(d, workspace);
     const int R = d.B * d.T;
@@ -211,7 +213,27 @@ df2_status select_checked(const df2_dims &d, const void *hidden, const void *W_v
     DF2_CUDA(profile_mark(t_profile_end, st));
     HostMirrors m = mirrors;
     m.status_dev = w.status;
-    return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st, m);
+    return finish(d, w, n_split, g, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, st, m, walk);
+}
+
+// Checks the walk options of dflash2_select_walk and turns them into the finish kernel's.
+df2_status walk_opts_of(const df2_walk_opts *o, WalkOpts *out)
+{
+    *out = WalkOpts{};
+    if (!o)
+        return DF2_OK;
+    if (!(o->temperature > 0.f) || !std::isfinite(o->temperature) || std::isnan(o->p_min))
+        return DF2_ERR_INVALID_ARG;
+    if ((o->uniforms && !aligned(o->uniforms, 4)) || (o->n_draft && !aligned(o->n_draft, 4)) ||
+        (o->confidence && !aligned(o->confidence, 4)))
+        return DF2_ERR_INVALID_ARG;
+    out->sample = true;
+    out->temperature = o->temperature;
+    out->p_min = o->p_min;
+    out->uniforms = o->uniforms;
+    out->n_draft = o->n_draft;
+    out->confidence = o->confidence;
+    return DF2_OK;
 }
 
 // Device-visible address of a caller's host buffer if it is page-locked memory mapped into
@@ -284,6 +306,24 @@ df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *
     cudaGetLastError();  // clear a stale error so the status reflects this call
     return select_checked(d, hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids,
                           topk_logits, gate, workspace, static_cast<cudaStream_t>(stream));
+}
+
+df2_status dflash2_select_walk(const df2_dims *dims, const df2_walk_opts *walk, const void *hidden,
+                               const void *W_vocab, const void *W_sel, const void *pred_cb, const void *succ_cb,
+                               const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
+                               float *topk_logits, float *gate, void *workspace, size_t workspace_bytes, void *stream)
+{
+    DF2_TRY(check_dims(dims));
+    const df2_dims d = *dims;
+    WalkOpts opts;
+    DF2_TRY(walk_opts_of(walk, &opts));
+    if (!hidden || !W_vocab || !aligned(hidden, 16) || !aligned(W_vocab, 16))
+        return DF2_ERR_INVALID_ARG;
+    DF2_TRY(check_tail_pointers(W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids, topk_logits, gate));
+    DF2_TRY(check_workspace(d, workspace, workspace_bytes));
+    cudaGetLastError();
+    return select_checked(d, hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, lattice, draft_ids, topk_ids,
+                          topk_logits, gate, workspace, static_cast<cudaStream_t>(stream), HostMirrors{}, opts);
 }
 
 size_t dflash2_select_host_workspace_bytes(const df2_dims *dims)
@@ -555,6 +595,6 @@ const char *dflash2_status_string(df2_status status)
     }
 }
 
-int32_t dflash2_version(void) { return 200; }
+int32_t dflash2_version(void) { return 300; }
 
 }  // extern "C"

@@ -12,8 +12,10 @@
 //      meanwhile fetch the gate row;
 //   2. the lattice row (lattice.cuh), plus the walk's choice for every predecessor row;
 //   3. the CTA counts itself done for sequence b; the last CTA of the sequence loads the
-//      T choice rows and candidate ids into shared memory and follows j_t = best[t][j_(t-1)].
-//      The counter returns to zero.
+//      T choice rows and candidate ids into shared memory and follows j_t = best[t][j_(t-1)]
+//      -- or, when the caller asked for confidences, a p_min stop or sampling, one warp walks
+//      the sequence's rows with the softmax of each row it reads (walk_sample_rows).  The
+//      counter returns to zero.
 // Launched with programmatic stream serialisation: its prologue overlaps the tail of the
 // kernel that produced the lists, and griddep_wait() orders the reads after it (the anchor,
 // which no earlier kernel of the call writes, is read before).
@@ -49,6 +51,11 @@ struct FinishArgs {
     int32_t *draft_mirror;
     const uint32_t *status;         // device status word, copied to status_mirror if set
     uint32_t *status_mirror;
+    int sample_walk;                // the confidence / p_min / sampling walk instead of the greedy one
+    float temperature, p_min;
+    const float *uniforms;          // [B*T] or null
+    int32_t *n_draft;               // [B] or null
+    float *confidence;              // [B*T] or null
 };
 
 constexpr int kFinishThreads = 128;
@@ -185,7 +192,14 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
     const float *rows = a.lattice + r0 * width;
     int32_t *draft = a.draft + r0;
     int32_t *draft_mirror = a.draft_mirror ? a.draft_mirror + r0 : nullptr;
-    if (a.walk_in_smem) {
+    if (a.sample_walk) {
+        // the confidence of each step needs the whole row the walk reads: one warp walks the
+        // rows through L2, with the same device code as the stand-alone sampling walk
+        if (warp == 0)
+            walk_sample_rows<true>(a.T, k, width, rows, a.temperature, a.p_min, a.uniforms ? a.uniforms + r0 : nullptr,
+                                   draft, draft_mirror, a.n_draft ? a.n_draft + b : nullptr,
+                                   a.confidence ? a.confidence + r0 : nullptr);
+    } else if (a.walk_in_smem) {
         int *sb = reinterpret_cast<int *>(smem);     // [T][k] choices
         int *sid = sb + a.T * k;                     // [T][k] candidate ids
         for (int i = threadIdx.x; i < a.T * k; i += blockDim.x) {
@@ -252,9 +266,15 @@ cudaError_t launch_finish(int B, int T, int k, int V, int D, int KP, int n_split
                           const int32_t *pid, const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
                           const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
                           float *topk_vals, int32_t *best, unsigned *counters, const HostMirrors &mirrors,
-                          cudaStream_t stream)
+                          const WalkOpts &walk, cudaStream_t stream)
 {
     FinishArgs a{};
+    a.sample_walk = walk.sample ? 1 : 0;
+    a.temperature = walk.temperature;
+    a.p_min = walk.p_min;
+    a.uniforms = walk.uniforms;
+    a.n_draft = walk.n_draft;
+    a.confidence = walk.confidence;
     a.lattice_mirror = mirrors.lattice;
     a.draft_mirror = mirrors.draft;
     a.status = mirrors.status_dev;

@@ -69,6 +69,18 @@ struct HostMirrors {
     const uint32_t *status_dev = nullptr;
 };
 
+// The walk the finish kernel runs: with `sample` false the greedy walk over each row's stored
+// argmax (no confidence); otherwise the walk with the chosen transition's softmax confidence,
+// the p_min stop and, given uniforms, inverse-CDF sampling (walk_sample_rows).
+struct WalkOpts {
+    bool sample = false;
+    float temperature = 1.f;
+    float p_min = 0.f;
+    const float *uniforms = nullptr;  // [B*T] in [0, 1), or null: greedy
+    int32_t *n_draft = nullptr;       // [B] or null
+    float *confidence = nullptr;      // [B*T] or null
+};
+
 // Everything after the lists in one launch (programmatic dependent launch): merge of
 // the [R, n_split, KP] lists, lattice rows, and the walk by the last CTA of each
 // sequence (best [R, k] is scratch for the walk's choices).  counters [B] must be zero
@@ -78,7 +90,7 @@ cudaError_t launch_finish(int B, int T, int k, int V, int D, int KP, int n_split
                           const int32_t *pid, const float *gate, const uint16_t *pred_cb, const uint16_t *succ_cb,
                           const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
                           float *topk_vals, int32_t *best, unsigned *counters, const HostMirrors &mirrors,
-                          cudaStream_t stream);
+                          const WalkOpts &walk, cudaStream_t stream);
 
 // Packed lattice rows [B*T, k + k*k] from candidates, unary scores, gate and codebooks.
 cudaError_t launch_lattice(int B, int T, int k, int V, int D, const int32_t *topk_ids, const float *topk_vals,

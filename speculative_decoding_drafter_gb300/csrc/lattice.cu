@@ -54,13 +54,8 @@ __global__ void __launch_bounds__(kLatticeThreads) walk_kernel(int B, int T, int
     walk_rows<true>(T, k, width, lattice + static_cast<long long>(b) * T * width, draft + static_cast<long long>(b) * T);
 }
 
-// One warp per sequence: the walk with the chosen transition's softmax confidence,
-// the p_min early stop and, when `uniforms` is given, inverse-CDF sampling from the
-// same scores.  "DFlash2 Lands in llama.cpp", section "p_min Means Something Different
-// Under DFlash2": the confidence is the softmax of the current transition row at the
-// chosen candidate, and the walk stops when it falls below p_min.  "DFlash 2: Keep
-// Drafting Parallel", section "A Lightweight Path Selector": sampling draws from the
-// same scores.
+// One warp per sequence: the walk with confidence, p_min stop and optional sampling
+// (walk_sample_rows), over a lattice a previous launch wrote.
 __global__ void __launch_bounds__(kLatticeThreads)
     walk_sample_kernel(int B, int T, int k, const float *__restrict__ lattice, float temperature, float p_min,
                        const float *__restrict__ uniforms, int32_t *__restrict__ draft, int32_t *__restrict__ n_draft,
@@ -70,68 +65,13 @@ __global__ void __launch_bounds__(kLatticeThreads)
         griddep_launch_dependents();
     griddep_wait();  // launched as a programmatic dependent
     const int b = blockIdx.x * kWarps + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
     if (b >= B)
         return;
     const long long width = k + static_cast<long long>(k) * k;
-    int jp = 0;
-    int n = T;
-    bool stopped = false;
-    for (int t = 0; t < T; ++t) {
-        const long long r = static_cast<long long>(b) * T + t;
-        if (stopped) {
-            if (lane == 0) {
-                draft[r] = -1;
-                if (confidence)
-                    confidence[r] = 0.f;
-            }
-            continue;
-        }
-        const float *row = lattice + r * width;
-        const float x = lane < k ? row[k + jp * k + lane] : -INFINITY;
-        // argmax (first maximum) and maximum
-        float mx = x;
-        int jm = lane < k ? lane : 0x7fffffff;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ox = __shfl_xor_sync(kFullMask, mx, off);
-            const int oj = __shfl_xor_sync(kFullMask, jm, off);
-            const bool take = ranks_before(ox, oj, mx, jm);
-            mx = take ? ox : mx;
-            jm = take ? oj : jm;
-        }
-        const float e = lane < k ? expf((x - mx) / temperature) : 0.f;
-        float pre = e;  // inclusive prefix sum over lanes
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float o = __shfl_up_sync(kFullMask, pre, off);
-            if (lane >= off)
-                pre += o;
-        }
-        const float z = __shfl_sync(kFullMask, pre, 31);
-        int pick = jm;
-        if (uniforms) {
-            const float target = uniforms[r] * z;
-            const unsigned over = __ballot_sync(kFullMask, lane < k && pre > target);
-            const unsigned live = __ballot_sync(kFullMask, e > 0.f);
-            pick = over ? __ffs(over) - 1 : 31 - __clz(live);
-        }
-        const float p = __shfl_sync(kFullMask, e, pick) / z;
-        if (lane == 0 && confidence)
-            confidence[r] = p;
-        if (p < p_min) {
-            stopped = true;
-            n = t;
-            if (lane == 0)
-                draft[r] = -1;
-        } else {
-            jp = pick;
-            if (lane == 0)
-                draft[r] = static_cast<int32_t>(row[pick]);
-        }
-    }
-    if (lane == 0 && n_draft)
-        n_draft[b] = n;
+    const long long r0 = static_cast<long long>(b) * T;
+    walk_sample_rows<false>(T, k, width, lattice + r0 * width, temperature, p_min, uniforms ? uniforms + r0 : nullptr,
+                            draft + r0, nullptr, n_draft ? n_draft + b : nullptr,
+                            confidence ? confidence + r0 : nullptr);
 }
 
 template <int KP>

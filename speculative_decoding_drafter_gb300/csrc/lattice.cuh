@@ -322,4 +322,89 @@ __device__ __forceinline__ void walk_rows(int T, int k, long long width, const f
     }
 }
 
+// One sequence's walk with the chosen transition's softmax confidence, the p_min early stop
+// and, when `uniforms` is given, inverse-CDF sampling from the same scores; one warp.
+// "DFlash2 Lands in llama.cpp", section "p_min Means Something Different Under DFlash2": the
+// confidence is the softmax of the current transition row at the chosen candidate, and the
+// walk stops when it falls below p_min.  "DFlash 2: Keep Drafting Parallel", section "A
+// Lightweight Path Selector": sampling draws from the same scores.
+// rows: the sequence's T packed rows (stride `width` floats); uniforms, draft, confidence:
+// its T entries (uniforms and confidence may be null); n_draft: its count (may be null);
+// draft_mirror: a second copy of the draft (may be null).  kGlobal reads the rows through L2
+// (rows written by other CTAs of the same grid).
+template <bool kGlobal>
+__device__ __forceinline__ void walk_sample_rows(int T, int k, long long width, const float *rows, float temperature,
+                                                 float p_min, const float *uniforms, int32_t *draft,
+                                                 int32_t *draft_mirror, int32_t *n_draft, float *confidence)
+{
+    const int lane = threadIdx.x & 31;
+    int jp = 0;
+    int n = T;
+    bool stopped = false;
+    for (int t = 0; t < T; ++t) {
+        if (stopped) {
+            if (lane == 0) {
+                draft[t] = -1;
+                if (draft_mirror)
+                    draft_mirror[t] = -1;
+                if (confidence)
+                    confidence[t] = 0.f;
+            }
+            continue;
+        }
+        const float *row = rows + static_cast<long long>(t) * width;
+        const float *px = row + k + jp * k + lane;
+        const float x = lane < k ? (kGlobal ? __ldcg(px) : *px) : -INFINITY;
+        // argmax (first maximum) and maximum
+        float mx = x;
+        int jm = lane < k ? lane : 0x7fffffff;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ox = __shfl_xor_sync(kFullMask, mx, off);
+            const int oj = __shfl_xor_sync(kFullMask, jm, off);
+            const bool take = ranks_before(ox, oj, mx, jm);
+            mx = take ? ox : mx;
+            jm = take ? oj : jm;
+        }
+        const float e = lane < k ? expf((x - mx) / temperature) : 0.f;
+        float pre = e;  // inclusive prefix sum over lanes
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float o = __shfl_up_sync(kFullMask, pre, off);
+            if (lane >= off)
+                pre += o;
+        }
+        const float z = __shfl_sync(kFullMask, pre, 31);
+        int pick = jm;
+        if (uniforms) {
+            const float target = uniforms[t] * z;
+            const unsigned over = __ballot_sync(kFullMask, lane < k && pre > target);
+            const unsigned live = __ballot_sync(kFullMask, e > 0.f);
+            pick = over ? __ffs(over) - 1 : 31 - __clz(live);
+        }
+        const float p = __shfl_sync(kFullMask, e, pick) / z;
+        if (lane == 0 && confidence)
+            confidence[t] = p;
+        if (p < p_min) {
+            stopped = true;
+            n = t;
+            if (lane == 0) {
+                draft[t] = -1;
+                if (draft_mirror)
+                    draft_mirror[t] = -1;
+            }
+        } else {
+            jp = pick;
+            if (lane == 0) {
+                const int32_t id = static_cast<int32_t>(kGlobal ? __ldcg(row + pick) : row[pick]);
+                draft[t] = id;
+                if (draft_mirror)
+                    draft_mirror[t] = id;
+            }
+        }
+    }
+    if (lane == 0 && n_draft)
+        *n_draft = n;
+}
+
 }  // namespace df2

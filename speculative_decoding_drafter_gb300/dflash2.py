@@ -23,7 +23,7 @@ __all__ = [
     "dflash2_walk", "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "Workspace",
     "dflash2_profile_events", "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv",
     "ConvDims", "EXPORTED_SYMBOLS", "dflash2_select_host", "dflash2_select_host_workspace_bytes", "HostWorkspace",
-    "SelectHostPlan", "dflash2_selftest_wait_timeout",
+    "SelectHostPlan", "dflash2_selftest_wait_timeout", "WalkOpts", "dflash2_select_walk",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -31,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "dflash2_lm_head_logits", "dflash2_topk", "dflash2_gate", "dflash2_lattice", "dflash2_walk",
     "dflash2_check_device_status", "dflash2_status_string", "dflash2_version", "dflash2_profile_events",
     "dflash2_topk_noalloc", "dflash2_walk_sample", "dflash2_dynamic_conv", "dflash2_select_host",
-    "dflash2_select_host_workspace_bytes", "dflash2_selftest_wait_timeout",
+    "dflash2_select_host_workspace_bytes", "dflash2_selftest_wait_timeout", "dflash2_select_walk",
 )
 
 
@@ -43,6 +43,12 @@ class DFlash2Error(RuntimeError):
 
 class ConvDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("T", ctypes.c_int32), ("C", ctypes.c_int32), ("G", ctypes.c_int32)]
+
+
+class WalkOpts(ctypes.Structure):
+    """df2_walk_opts: temperature, p_min, uniforms [B, T] (or NULL: greedy), n_draft [B], confidence [B, T]."""
+    _fields_ = [("temperature", ctypes.c_float), ("p_min", ctypes.c_float), ("uniforms", ctypes.c_void_p),
+                ("n_draft", ctypes.c_void_p), ("confidence", ctypes.c_void_p)]
 
 
 class Dims(ctypes.Structure):
@@ -89,6 +95,7 @@ def library(path: str | None = None):
                 "dflash2_select_host": (I, [D, P, P, P, P, P, P, P, P, P, P, S, P]),
                 "dflash2_select_host_workspace_bytes": (S, [D]),
                 "dflash2_selftest_wait_timeout": (I, [ctypes.c_uint32, P, S, P]),
+                "dflash2_select_walk": (I, [D, ctypes.POINTER(WalkOpts), P, P, P, P, P, P, P, P, P, P, P, P, S, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(lib, name)
@@ -245,6 +252,36 @@ def dflash2_select(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: 
         _ptr(gate, torch.float32, (R, d.D), "gate"), ws.ptr, ws.nbytes, _stream(stream))
     _check(st, "dflash2_select")
     return lattice, draft_ids
+
+
+def dflash2_select_walk(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, temperature: float = 1.0,
+                        p_min: float = 0.0, uniforms=None, lattice=None, draft_ids=None, n_draft=None,
+                        confidence=None, topk_ids=None, topk_logits=None, gate=None, workspace=None, stream=None):
+    """Whole selector head with the confidence / p_min / sampling walk in the same launches.
+
+    Returns (lattice, draft_ids [B, T] with -1 from a stop on, n_draft int32 [B], confidence float32 [B, T])."""
+    d = _dims_of(hidden, W_vocab, W_sel, pred_cb, k, T)
+    dev = hidden.device
+    R = d.B * d.T
+    lattice = lattice if lattice is not None else torch.empty((R, k + k * k), dtype=torch.float32, device=dev)
+    draft_ids = draft_ids if draft_ids is not None else torch.empty((d.B, T), dtype=torch.int32, device=dev)
+    n_draft = n_draft if n_draft is not None else torch.empty((d.B,), dtype=torch.int32, device=dev)
+    confidence = confidence if confidence is not None else torch.empty((d.B, T), dtype=torch.float32, device=dev)
+    ws = _workspace(workspace, d, dev)
+    opts = WalkOpts(float(temperature), float(p_min), _ptr(uniforms, torch.float32, (d.B, T), "uniforms"),
+                    _ptr(n_draft, torch.int32, (d.B,), "n_draft"),
+                    _ptr(confidence, torch.float32, (d.B, T), "confidence"))
+    bf = torch.bfloat16
+    st = library().dflash2_select_walk(
+        ctypes.byref(d), ctypes.byref(opts), _ptr(hidden, bf, (R, d.H), "hidden"),
+        _ptr(W_vocab, bf, (d.V, d.H), "W_vocab"), _ptr(W_sel, bf, (d.D, d.H), "W_sel"),
+        _ptr(pred_cb, bf, (d.V, d.D), "pred_cb"), _ptr(succ_cb, bf, (d.V, d.D), "succ_cb"),
+        _ptr(anchor, torch.int32, (d.B,), "anchor"), _ptr(lattice, torch.float32, (R, k + k * k), "lattice"),
+        _ptr(draft_ids, torch.int32, (d.B, T), "draft_ids"), _ptr(topk_ids, torch.int32, (R, k), "topk_ids"),
+        _ptr(topk_logits, torch.float32, (R, k), "topk_logits"), _ptr(gate, torch.float32, (R, d.D), "gate"),
+        ws.ptr, ws.nbytes, _stream(stream))
+    _check(st, "dflash2_select_walk")
+    return lattice, draft_ids, n_draft, confidence
 
 
 def _select_host_args(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k, T, lattice_host,

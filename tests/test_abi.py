@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_version_and_status_strings(lib):
     from speculative_decoding_drafter_gb300 import dflash2
 
-    assert dflash2.dflash2_version() == 200
+    assert dflash2.dflash2_version() == 300
     for s in range(6):
         assert len(dflash2.dflash2_status_string(s)) >= 2
     assert dflash2.dflash2_status_string(99) == "unknown status"
@@ -84,6 +84,29 @@ def test_select_rejects_bad_arguments_before_any_cuda_call(lib):
     assert _select(lib, dims(), {}, ws=0x100010) == DF2_ERR_WORKSPACE  # not 256-byte aligned
     assert _select(lib, dims(), {}, ws_bytes=1024) == DF2_ERR_WORKSPACE
     assert lib.dflash2_select(None, 0, 0, 0, 0, 0, 0, 0, 0, None, None, None, 0, 0, None) == DF2_ERR_INVALID_ARG
+
+
+def test_select_walk_rejects_bad_options_before_any_cuda_call(lib):
+    # Pointer values below are never dereferenced: every case fails validation first.
+    from speculative_decoding_drafter_gb300.dflash2 import WalkOpts
+
+    names = ["hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb", "anchor", "lattice", "draft"]
+    p = [0x200000 + 0x1000 * i for i in range(len(names))]
+
+    def call(opts, d=None, ws=0x100000):
+        d = d or dims()
+        return lib.dflash2_select_walk(ctypes.byref(d), None if opts is None else ctypes.byref(opts), *p, None, None,
+                                       None, ws, 1 << 40, None)
+
+    assert call(WalkOpts(0.0, 0.5, None, None, None)) == DF2_ERR_INVALID_ARG  # temperature must be > 0
+    assert call(WalkOpts(float("inf"), 0.5, None, None, None)) == DF2_ERR_INVALID_ARG
+    assert call(WalkOpts(1.0, float("nan"), None, None, None)) == DF2_ERR_INVALID_ARG
+    assert call(WalkOpts(1.0, 0.5, 0x3002, None, None)) == DF2_ERR_INVALID_ARG  # uniforms not 4-byte aligned
+    assert call(WalkOpts(1.0, 0.5, None, 0x3001, None)) == DF2_ERR_INVALID_ARG
+    assert call(WalkOpts(1.0, 0.5, None, None, 0x3003)) == DF2_ERR_INVALID_ARG
+    assert call(WalkOpts(1.0, 0.5, None, None, None), d=dims(k=33)) == DF2_ERR_UNSUPPORTED
+    assert call(WalkOpts(1.0, 0.5, None, None, None), ws=0x100010) == DF2_ERR_WORKSPACE
+    assert call(None, ws=0) == DF2_ERR_WORKSPACE  # NULL options: dflash2_select's checks
 
 
 def test_stage_entry_points_reject_bad_arguments(lib):

@@ -577,20 +577,13 @@ def _softmax64(row, tau):
     return e / e.sum()
 
 
-@pytest.mark.parametrize("B,T,k,tau,p_min", [(5, 16, 8, 1.0, 0.0), (4, 16, 16, 0.7, 0.2), (3, 9, 32, 1.3, 0.05),
-                                             (6, 8, 1, 1.0, 0.5), (64, 16, 16, 1.0, 0.3)])
-@pytest.mark.parametrize("sampling", [False, True])
-def test_walk_sample_stage(B, T, k, tau, p_min, sampling):
-    rng = np.random.default_rng(B * 100 + k + int(sampling))
-    lat = np.zeros((B * T, k + k * k), np.float32)
-    lat[:, :k] = rng.integers(0, 1 << 20, size=(B * T, k))
-    lat[:, k:] = (rng.standard_normal((B * T, k * k)) * 1.5).astype(np.float32)
-    for b in range(B):
-        lat[b * T, k:] = np.tile(lat[b * T, k:2 * k], k)
-    u = rng.random((B, T)).astype(np.float32) if sampling else None
-    d, n, c = df.dflash2_walk_sample(dev(lat), B, T, k, temperature=tau, p_min=p_min,
-                                     uniforms=None if u is None else dev(u))
-    d, n, c = host(d), host(n), host(c)
+def compare_walk_sample(lat, B, T, k, tau, p_min, u, d, n, c):
+    """The GPU's walk with confidence / p_min / sampling (draft d, n_draft n, confidence c) against
+    the oracle's walk over the same float32 lattice.  Float32 probabilities on the GPU, double in
+    the oracle: a step whose confidence lies within eps of p_min, or (sampling) whose uniform lies
+    within eps of a cumulative boundary, may go either way and ends the comparison of its
+    sequence.  Returns (steps compared, steps the oracle walked)."""
+    sampling = u is not None
     wd, wn, wc = oracle.walk_sample(lat, B, T, k, temperature=tau, p_min=p_min, uniforms=u)
     eps = 1e-5
     compared = 0
@@ -617,7 +610,52 @@ def test_walk_sample_stage(B, T, k, tau, p_min, sampling):
         else:
             assert n[b] == wn[b] == T
     walked = int(np.minimum(wn + 1, T).sum())  # steps the oracle takes, the stopping step included
+    return compared, walked
+
+
+@pytest.mark.parametrize("B,T,k,tau,p_min", [(5, 16, 8, 1.0, 0.0), (4, 16, 16, 0.7, 0.2), (3, 9, 32, 1.3, 0.05),
+                                             (6, 8, 1, 1.0, 0.5), (64, 16, 16, 1.0, 0.3)])
+@pytest.mark.parametrize("sampling", [False, True])
+def test_walk_sample_stage(B, T, k, tau, p_min, sampling):
+    rng = np.random.default_rng(B * 100 + k + int(sampling))
+    lat = np.zeros((B * T, k + k * k), np.float32)
+    lat[:, :k] = rng.integers(0, 1 << 20, size=(B * T, k))
+    lat[:, k:] = (rng.standard_normal((B * T, k * k)) * 1.5).astype(np.float32)
+    for b in range(B):
+        lat[b * T, k:] = np.tile(lat[b * T, k:2 * k], k)
+    u = rng.random((B, T)).astype(np.float32) if sampling else None
+    d, n, c = df.dflash2_walk_sample(dev(lat), B, T, k, temperature=tau, p_min=p_min,
+                                     uniforms=None if u is None else dev(u))
+    compared, walked = compare_walk_sample(lat, B, T, k, tau, p_min, u, host(d), host(n), host(c))
     assert compared >= 0.8 * walked, (compared, walked)
+
+
+@pytest.mark.parametrize("mode,tau,p_min", [("greedy", 1.0, 0.0), ("greedy_pmin", 1.0, 0.3), ("sampling", 0.8, 0.1)])
+def test_select_walk_fuses_confidence_pmin_and_sampling(case, mode, tau, p_min):
+    """dflash2_select_walk: the p_min stop, the confidences and the sampling draw come out of the
+    selector call itself (the finish kernel's walk), at full size on every config.  The lattice is
+    the plain call's bit for bit, the walk's outputs are those of the stand-alone sampling walk on
+    that lattice bit for bit, and they agree with the oracle's walk."""
+    cfg, d = case["cfg"], case["d"]
+    B, T, k = cfg.B, cfg.T, cfg.k
+    rng = np.random.default_rng(cfg.R + k)
+    u = rng.random((B, T)).astype(np.float32) if mode == "sampling" else None
+    lat, draft, n, conf = df.dflash2_select_walk(d["hidden"], d["W_vocab"], d["W_sel"], d["pred_cb"], d["succ_cb"],
+                                                 d["anchor"], k, T, temperature=tau, p_min=p_min,
+                                                 uniforms=None if u is None else dev(u), workspace=case["ws"])
+    torch.cuda.synchronize()
+    df.dflash2_check_device_status(case["ws"])
+    assert np.array_equal(host(lat).view(np.uint32), case["lat"].view(np.uint32))
+    d2, n2, c2 = df.dflash2_walk_sample(lat, B, T, k, temperature=tau, p_min=p_min,
+                                        uniforms=None if u is None else dev(u))
+    assert np.array_equal(host(draft), host(d2)) and np.array_equal(host(n), host(n2))
+    assert np.array_equal(host(conf).view(np.uint32), host(c2).view(np.uint32))
+    if mode == "greedy":
+        assert np.array_equal(host(draft), case["draft"]) and np.all(host(n) == T)
+    compared, walked = compare_walk_sample(host(lat), B, T, k, tau, p_min, u, host(draft), host(n), host(conf))
+    assert compared >= 0.8 * walked, (compared, walked)
+    report(f"{cfg.name}: select_walk ({mode}, temperature {tau}, p_min {p_min}): {compared} of {walked} walked steps "
+           f"equal to the oracle's walk on the call's lattice; {int(host(n).sum())} tokens drafted")
 
 
 def test_walk_sample_greedy_reproduces_the_select_draft(case):
@@ -628,6 +666,28 @@ def test_walk_sample_greedy_reproduces_the_select_draft(case):
     assert np.all(host(n) == cfg.T)
     conf = host(c)
     assert np.all((conf > 0) & (conf <= 1.0 + 1e-6))
+
+
+@pytest.mark.parametrize("B,T,H,V,k,D", [(3, 7, 200, 1013, 5, 24), (2, 9, 136, 5000, 32, 64), (3, 5, 128, 777, 1, 16),
+                                         (2, 300, 64, 5000, 32, 16), (20, 16, 256, 20000, 16, 64)])
+def test_select_walk_edge_shapes(B, T, H, V, k, D):
+    """The fused walk on ragged shapes, k = 1 and k = 32, and sequences long enough that the greedy
+    walk's choice table would not fit shared memory: same bits as the stand-alone sampling walk on
+    the call's lattice, and the oracle's walk agrees."""
+    cfg, x = small_case(B, T, H, V, k, D, seed=B + T + k + 77)
+    dd = {n: dev_bf16(x[n]) for n in ("hidden", "W_vocab", "W_sel", "pred_cb", "succ_cb")}
+    rng = np.random.default_rng(B * T + k)
+    for tau, p_min, u in ((1.0, 0.25, None), (1.2, 0.05, rng.random((B, T)).astype(np.float32))):
+        lat, draft, n, conf = df.dflash2_select_walk(dd["hidden"], dd["W_vocab"], dd["W_sel"], dd["pred_cb"],
+                                                     dd["succ_cb"], dev(x["anchor"]), k, T, temperature=tau,
+                                                     p_min=p_min, uniforms=None if u is None else dev(u))
+        d2, n2, c2 = df.dflash2_walk_sample(lat, B, T, k, temperature=tau, p_min=p_min,
+                                            uniforms=None if u is None else dev(u))
+        torch.cuda.synchronize()
+        assert np.array_equal(host(draft), host(d2)) and np.array_equal(host(n), host(n2))
+        assert np.array_equal(host(conf).view(np.uint32), host(c2).view(np.uint32))
+        compared, walked = compare_walk_sample(host(lat), B, T, k, tau, p_min, u, host(draft), host(n), host(conf))
+        assert compared >= 0.8 * walked, (compared, walked)
 
 
 # ---------------------------------------------------------------- dynamic local convolution
