@@ -23,7 +23,7 @@
 // Two row tiles per CTA (beyond 128 rows) halve what an SM takes in per MMA flop: 64 KB of
 // A and B per 2 x 128x256x64 block instead of 48 KB per 128x256x64, which is what limits
 // the tensor pipe when all SMs stream.
-// CTA pairs (129 to 512 rows): the two row tiles go to a cluster of two CTAs on two SMs
+// CTA pairs (129 to 1024 rows): the two row tiles go to a cluster of two CTAs on two SMs
 // instead.  The even CTA issues tcgen05.mma.cta_group::2 (M = 256); each CTA loads its
 // 128-row A tile and a 128-row box of B at its half of the chunk, both completing on the
 // even CTA's barriers, and the commits arrive on both CTAs' barriers.  An SM then takes in
@@ -689,11 +689,14 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     // the next chunk's MMAs (two buffers); in one CTA (mt = 2) the two tiles' accumulators
     // fill TMEM (one buffer) and the MMA waits for the epilogue.  Both take 64 KB of operands
     // per stage in two TMA operations (three stages).  Measured on GB300 (same bits): pairs
-    // 464.4 -> 429.6 us per call at 512 rows; at 1024 rows, where the kernel runs long enough
-    // to settle at the power cap, 1760.1 -> 1772.7 us, so larger row counts stay in one CTA.
+    // 464.4 -> 429.6 us per call at 512 rows; at 1024 rows, in one process with the two
+    // kernels' calls interleaved in blocks of ten (20 rounds), 1686.9 -> 1613.9 us per LM head.
+    // In one CTA the MMA warp waited 6.9% of its cycles for the epilogue and 8.0% for TMA
+    // (cycle counters in an instrumented copy); as pairs, 0.2% and 14.6%.  Beyond 1024 rows
+    // (not measured) two tiles stay in one CTA.
     const bool two_tiles = args.bn == BN && args.row_tiles >= 2;
     // pairs read A and B through 3-D views whose K-blocks must not straddle rows
-    args.pair = two_tiles && args.row_tiles <= 4 && K % BK == 0 ? 1 : 0;
+    args.pair = two_tiles && args.row_tiles <= 8 && K % BK == 0 ? 1 : 0;
     if (args.pair)
         args.kbs = 2;
     args.mt = two_tiles && !args.pair ? 2 : 1;

@@ -782,8 +782,21 @@ def _random_pair_shapes(n, seed):
     return out
 
 
+def _random_wide_pair_shapes(n, seed):
+    """513 to 1024 rows with H a multiple of 64: CTA pairs over up to eight row tiles (four pair
+    row groups), an odd tile count (the last pair's second tile empty), ragged last tiles."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        k = 32 if i == 0 else int(rng.integers(1, 33))
+        T = int(rng.integers(1, 18))
+        B = int(rng.integers(-(-513 // T), 1024 // T + 1))
+        out.append((B, T, 64 * int(rng.integers(1, 25)), int(rng.integers(k, 7001)), k, 8 * int(rng.integers(1, 33))))
+    return out
+
+
 @pytest.mark.parametrize("B,T,H,V,k,D", _random_shapes(24, 2024) + _random_multi_tile_shapes(8, 2025) +
-                         _random_pair_shapes(8, 2026))
+                         _random_pair_shapes(8, 2026) + _random_wide_pair_shapes(6, 2027))
 def test_select_random_shapes(B, T, H, V, k, D):
     """Seeded random shapes across the limits: the fused path against the oracle under the same rules."""
     cfg, x = small_case(B, T, H, V, k, D, seed=B * 1000 + T * 10 + k)
