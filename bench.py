@@ -18,6 +18,7 @@ rank's time.  --impl reference times the CPU oracle (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -139,16 +140,23 @@ def recorded_traffic(cfg):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs.
+
+    Each sample carries nvidia-smi's timestamp; mark_start() / mark_end() bracket the timed
+    region on the host clock, and window() keeps the samples inside it (a region shorter
+    than the 20 ms sampling period keeps the first sample after its start)."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,timestamp")
+    TS_FORMAT = "%Y/%m/%d %H:%M:%S.%f"
 
     def __init__(self, device_id: str):
         self.device_id = device_id
         self.proc = None
         self.tmp = None
+        self.t_start = None
+        self.t_end = None
 
     def start(self):
         self.tmp = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
@@ -159,6 +167,12 @@ class ClockSampler:
         except OSError:
             self.proc = None
         time.sleep(0.3)
+
+    def mark_start(self):
+        self.t_start = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t_end = datetime.datetime.now()
 
     def stop(self):
         if self.proc is not None:
@@ -173,7 +187,28 @@ class ClockSampler:
         rows = [ln.strip().split(", ") for ln in self.tmp.read().splitlines() if ln.strip()]
         self.tmp.close()
         os.unlink(self.tmp.name)
-        return rows
+        return self.window(rows, self.t_start, self.t_end)
+
+    @classmethod
+    def window(cls, rows, t_start, t_end):
+        """The samples taken between t_start and t_end (datetimes on the host clock); if none, the
+        first sample after t_start; rows without a readable timestamp are kept only when no row
+        has one (an nvidia-smi without the field)."""
+        if t_start is None or t_end is None:
+            return rows
+        stamped = []
+        for r in rows:
+            try:
+                stamped.append((datetime.datetime.strptime(r[8].strip(), cls.TS_FORMAT), r))
+            except (IndexError, ValueError):
+                continue
+        if not stamped:
+            return rows
+        inside = [r for t, r in stamped if t_start <= t <= t_end]
+        if inside:
+            return inside
+        after = [r for t, r in stamped if t >= t_start]
+        return after[:1]
 
     @staticmethod
     def summarize(rows, t_first: int):
@@ -193,7 +228,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": "samples taken inside the timed region"}
 
 
 def device_id_for_smi(torch) -> str:
@@ -315,6 +350,7 @@ def timed_select(torch, df, cfg, d, steps: int, warmup: int, sampler=None, barri
     torch.cuda.synchronize()
     if sampler:
         sampler.start()
+        sampler.mark_start()
     start.record()
     for i in range(steps):
         if i % every == 0:
@@ -324,6 +360,8 @@ def timed_select(torch, df, cfg, d, steps: int, warmup: int, sampler=None, barri
         step()
     end.record()
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
     barrier()
     df.dflash2_profile_events(None, None)
     clock_rows = sampler.stop() if sampler else []
@@ -554,11 +592,14 @@ def run_conv(args, rank: int, world: int):
         dist.barrier()
     if sampler:
         sampler.start()
+        sampler.mark_start()
     start.record()
     for _ in range(args.steps):
         step()
     end.record()
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark_end()
     if dist is not None:
         dist.barrier()
     clock_rows = sampler.stop() if sampler else []
@@ -718,7 +759,9 @@ def run_walk(args, rank: int, world: int):
 
     sampler = ClockSampler(device_id_for_smi(torch))
     sampler.start()
+    sampler.mark_start()
     us = timed(sampled)
+    sampler.mark_end()
     clock_rows = sampler.stop()
     greedy_us = timed(greedy)
     sampled()

@@ -34,6 +34,26 @@ def test_clock_summary_median_max_and_reasons():
                                                    "samples": 0}
 
 
+def test_clock_samples_are_taken_from_the_timed_region_only():
+    import datetime
+
+    t0 = datetime.datetime(2026, 12, 2, 10, 0, 0)
+    ts = lambda ms: (t0 + datetime.timedelta(milliseconds=ms)).strftime(bench.ClockSampler.TS_FORMAT)[:-3]
+    rows = [row(2070, 2070) + [ts(-40)], row(2070, 2070) + [ts(-20)], row(1800, 2070, ["sw_power_cap"]) + [ts(5)],
+            row(1750, 2070, ["sw_power_cap"]) + [ts(25)], row(2070, 2070) + [ts(60)]]
+    inside = bench.ClockSampler.window(rows, t0, t0 + datetime.timedelta(milliseconds=30))
+    s = bench.ClockSampler.summarize(inside, 0)
+    assert s["samples"] == 2 and s["sm_mhz"] == 1775.0 and s["reasons"] == ["sw_power_cap"]
+    # a region shorter than the sampling period keeps the first sample after its start
+    short = bench.ClockSampler.window(rows, t0 + datetime.timedelta(milliseconds=6),
+                                      t0 + datetime.timedelta(milliseconds=8))
+    assert len(short) == 1 and short[0][0] == "1750"
+    # without marks (or without timestamps) every sample is kept
+    assert bench.ClockSampler.window(rows, None, None) == rows
+    bare = [r[:8] for r in rows]
+    assert bench.ClockSampler.window(bare, t0, t0) == bare
+
+
 def test_roofline_regime_of_each_workload():
     assert bench.roofline_bound(CONFIGS["8b_b1"], PEAKS) == "hbm"
     assert bench.roofline_bound(CONFIGS["27b_b8"], PEAKS) == "hbm"
