@@ -457,8 +457,16 @@ df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk
     const int R = d.B * d.T;
     const int kp = kp_for(d.k);
     int n_split = 0;
-    DF2_CUDA(launch_logits_topk_partial(logits, R, d.V, kp, w.pval, w.pid, &n_split, st));
-    DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, topk_ids, topk_logits, st));
+    // the bound slots (zero between calls, unused without the LM head) count each row's slices
+    TopkFinish fin;
+    fin.row_done = w.bound;
+    fin.k = d.k;
+    fin.ids = topk_ids;
+    fin.vals = topk_logits;
+    bool merged = false;
+    DF2_CUDA(launch_logits_topk_partial(logits, R, d.V, kp, w.pval, w.pid, &n_split, st, fin, &merged));
+    if (!merged)
+        DF2_CUDA(launch_topk_merge(w.pval, w.pid, R, n_split, kp, d.k, topk_ids, topk_logits, st));
     return DF2_OK;
 }
 

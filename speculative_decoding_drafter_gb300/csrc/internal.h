@@ -52,9 +52,21 @@ inline int lm_head_max_groups(long long R) { return static_cast<int>((R + 127) /
 cudaError_t launch_gemm_store(const void *A, const void *B, int R, int K, int N, float *out, long long ldo,
                               uint32_t *status, cudaStream_t stream);
 
-// Per-row partial top-KP of given float32 logits [R, V] over n_split column slices.
+// Optional finish of the top-k of given logits inside the slice launch: row_done [R] counters
+// (zero before, zero after), and where the rows' top-k go.
+struct TopkFinish {
+    unsigned *row_done = nullptr;
+    int k = 0;
+    int32_t *ids = nullptr;
+    float *vals = nullptr;
+};
+
+// Per-row partial top-KP of given float32 logits [R, V] over n_split column slices.  With
+// fin.row_done set, the launch may also merge the rows into fin.ids / fin.vals (the slice
+// kernel for few rows does): *merged (if not null) then says so and no merge launch is needed.
 cudaError_t launch_logits_topk_partial(const float *logits, int R, int V, int KP, float *pval, int32_t *pid,
-                                       int *n_split_out, cudaStream_t stream);
+                                       int *n_split_out, cudaStream_t stream, const TopkFinish &fin = TopkFinish{},
+                                       bool *merged = nullptr);
 
 // Merge [R, n_split, KP] partial lists into the top-k of each row (value desc, id asc).
 cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int n_split, int KP, int k,

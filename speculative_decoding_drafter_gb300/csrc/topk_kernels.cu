@@ -153,6 +153,75 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
     }
 }
 
+// Merges the n_split sorted lists of KP of row r (pval/pid, written by other CTAs: read
+// through L2) into the row's top-k, one warp.  Lane l merges whole lists l, l + 32, ... into
+// its own sorted top-KP; the lanes' lists are then combined by gathering the entries at or
+// above a bound on the row's KP-th best (bounded_merge), or, when more than 32 are, by the warp
+// butterfly.  (Offering every entry to one warp-wide list cost 12.7 us at 16 rows x 38 lists of
+// 8 and 30.5 us at 16 x 64 lists of 16, measured on GB300: each insertion is a chain of
+// dependent shuffles.)  s_mv / s_mi: 32 entries of shared memory for this warp.
+template <int KP>
+__device__ __forceinline__ void merge_row_lists(const float *pval, const int32_t *pid, int r, int n_split, int k,
+                                                int32_t *ids, float *vals, float *s_mv, int *s_mi)
+{
+    const int lane = threadIdx.x & 31;
+    if (n_split == 1) {
+        // one slice covered the whole row: its sorted list is the row's top-KP (the lane
+        // butterfly below would merge it with 31 lanes of empty entries)
+        if (lane < k) {
+            const long long o = static_cast<long long>(r) * KP + lane;
+            ids[static_cast<long long>(r) * k + lane] = __ldcg(pid + o);
+            vals[static_cast<long long>(r) * k + lane] = __ldcg(pval + o);
+        }
+        return;
+    }
+    float av[KP];
+    int ai[KP];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+        av[j] = -INFINITY;
+        ai[j] = INT_MAX;
+    }
+    const long long row_base = static_cast<long long>(r) * n_split * KP;
+    for (int list = lane; list < n_split; list += 32) {
+        const float4 *pv = reinterpret_cast<const float4 *>(pval + row_base + static_cast<long long>(list) * KP);
+        const int4 *pi = reinterpret_cast<const int4 *>(pid + row_base + static_cast<long long>(list) * KP);
+        float bv[KP];
+        int bi[KP];
+#pragma unroll
+        for (int q = 0; q < KP / 4; ++q) {
+            const float4 v4 = __ldcg(pv + q);
+            const int4 i4 = __ldcg(pi + q);
+            bv[4 * q] = v4.x;
+            bv[4 * q + 1] = v4.y;
+            bv[4 * q + 2] = v4.z;
+            bv[4 * q + 3] = v4.w;
+            bi[4 * q] = i4.x;
+            bi[4 * q + 1] = i4.y;
+            bi[4 * q + 2] = i4.z;
+            bi[4 * q + 3] = i4.w;
+        }
+        merge_top<KP>(av, ai, bv, bi);
+    }
+    float mv;
+    int mi;
+    if (!(KP <= 16 && bounded_merge<KP>(av, ai, s_mv, s_mi, mv, mi))) {
+        warp_merge_top<KP>(av, ai, 31);  // every lane now holds the row's top-KP
+        mv = -INFINITY;
+        mi = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < KP; ++j)
+            if (j == lane) {
+                mv = av[j];
+                mi = ai[j];
+            }
+    }
+    if (lane < k) {
+        ids[static_cast<long long>(r) * k + lane] = mi;
+        vals[static_cast<long long>(r) * k + lane] = mv;
+    }
+}
+
 // Few rows (a grid of one wave): one CTA per (row, 4096-column slice), a
 // thread holding 16 values in registers.  The per-warp list of the kernel above spends most of
 // its time in the chain of insertions while a list fills, which at 16 rows is the whole
@@ -162,13 +231,20 @@ __global__ void __launch_bounds__(kThreads) logits_topk_partial_kernel(const flo
 // therefore bounds the slice's KP-th best from below.  The values at or above tau (typically
 // a few dozen) are gathered in shared memory and warp 0 sorts them 32 at a time into the
 // slice's top-KP.  The gather holds every value of the slice, so no count can overflow it.
+// With row_done (one counter per row, zero before the launch and zero again after it) the
+// kernel also finishes the rows: the CTA that completes a row's last slice, found by an atomic
+// counter (nothing waits), merges the row's slice lists into ids / vals, so no merge launch
+// follows (measured on GB300 at 16 rows x 151936, k = 8: 14.3 us in two launches before).
 constexpr int kSmallPerThread = 16;                          // values per thread
 constexpr int kSmallCols = kThreads * kSmallPerThread;       // columns per CTA
 
 template <int KP>
 __global__ void __launch_bounds__(kThreads) logits_topk_small_kernel(const float *__restrict__ logits, int V,
                                                                      int n_split, float *__restrict__ pval,
-                                                                     int32_t *__restrict__ pid)
+                                                                     int32_t *__restrict__ pid,
+                                                                     unsigned *__restrict__ row_done, int k,
+                                                                     int32_t *__restrict__ ids,
+                                                                     float *__restrict__ vals)
 {
     if (threadIdx.x == 0)
         griddep_launch_dependents();
@@ -276,14 +352,24 @@ __global__ void __launch_bounds__(kThreads) logits_topk_small_kernel(const float
         pval[o] = bv;
         pid[o] = bi;
     }
+    if (!row_done)
+        return;
+    // the CTA that completes the row merges it (its list reaches L2 before it counts itself)
+    __threadfence();
+    __syncwarp();
+    unsigned last = 0;
+    if (lane == 0)
+        last = atomicAdd(row_done + r, 1u) == static_cast<unsigned>(n_split - 1);
+    if (!__shfl_sync(kFullMask, last, 0))
+        return;
+    __threadfence();
+    merge_row_lists<KP>(pval, pid, r, n_split, k, ids, vals, reinterpret_cast<float *>(s_v),
+                        reinterpret_cast<int *>(s_i));
+    if (lane == 0)
+        row_done[r] = 0u;
 }
 
-// One warp per row: merge n_split sorted lists of KP into the row's top-k.  Lane l merges
-// whole lists l, l + 32, ... into its own sorted top-KP; the lanes' lists are then combined
-// by gathering the entries at or above a bound on the row's KP-th best (bounded_merge), or,
-// when more than 32 are, by the warp butterfly.  (Offering every entry to one warp-wide list
-// cost 12.7 us at 16 rows x 38 lists of 8 and 30.5 us at 16 x 64 lists of 16, measured on
-// GB300: each insertion is a chain of dependent shuffles.)
+// One warp per row: merge n_split sorted lists of KP into the row's top-k (merge_row_lists).
 template <int KP>
 __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float *__restrict__ pval,
                                                               const int32_t *__restrict__ pid, int R, int n_split,
@@ -297,70 +383,16 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const float *__res
     __shared__ int s_mi[kWarps][32];
     const int warp = threadIdx.x >> 5;
     const int r = blockIdx.x * kWarps + warp;
-    const int lane = threadIdx.x & 31;
     if (r >= R)
         return;
-    if (n_split == 1) {
-        // one slice covered the whole row: its sorted list is the row's top-KP (the lane
-        // butterfly below would merge it with 31 lanes of empty entries)
-        if (lane < k) {
-            const long long o = static_cast<long long>(r) * KP + lane;
-            ids[static_cast<long long>(r) * k + lane] = __ldcg(pid + o);
-            vals[static_cast<long long>(r) * k + lane] = __ldcg(pval + o);
-        }
-        return;
-    }
-    float av[KP];
-    int ai[KP];
-#pragma unroll
-    for (int j = 0; j < KP; ++j) {
-        av[j] = -INFINITY;
-        ai[j] = INT_MAX;
-    }
-    const long long row_base = static_cast<long long>(r) * n_split * KP;
-    for (int list = lane; list < n_split; list += 32) {
-        const float4 *pv = reinterpret_cast<const float4 *>(pval + row_base + static_cast<long long>(list) * KP);
-        const int4 *pi = reinterpret_cast<const int4 *>(pid + row_base + static_cast<long long>(list) * KP);
-        float bv[KP];
-        int bi[KP];
-#pragma unroll
-        for (int q = 0; q < KP / 4; ++q) {
-            const float4 v4 = __ldcg(pv + q);
-            const int4 i4 = __ldcg(pi + q);
-            bv[4 * q] = v4.x;
-            bv[4 * q + 1] = v4.y;
-            bv[4 * q + 2] = v4.z;
-            bv[4 * q + 3] = v4.w;
-            bi[4 * q] = i4.x;
-            bi[4 * q + 1] = i4.y;
-            bi[4 * q + 2] = i4.z;
-            bi[4 * q + 3] = i4.w;
-        }
-        merge_top<KP>(av, ai, bv, bi);
-    }
-    float mv;
-    int mi;
-    if (!(KP <= 16 && bounded_merge<KP>(av, ai, s_mv[warp], s_mi[warp], mv, mi))) {
-        warp_merge_top<KP>(av, ai, 31);  // every lane now holds the row's top-KP
-        mv = -INFINITY;
-        mi = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < KP; ++j)
-            if (j == lane) {
-                mv = av[j];
-                mi = ai[j];
-            }
-    }
-    if (lane < k) {
-        ids[static_cast<long long>(r) * k + lane] = mi;
-        vals[static_cast<long long>(r) * k + lane] = mv;
-    }
+    merge_row_lists<KP>(pval, pid, r, n_split, k, ids, vals, s_mv[warp], s_mi[warp]);
 }
 
 template <int KP>
 cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32_t *pid, int *n_split_out,
-                           cudaStream_t stream)
+                           const TopkFinish &fin, bool *merged, cudaStream_t stream)
 {
+    *merged = false;
     // about one CTA per SM in total (one per row beyond), slices of at least 2048 columns.  Every
     // warp pays a warm-up of ~k (1 + ln(n / k)) list insertions over its n values, so long slices
     // win once the CTAs cover the SMs (measured on GB300: 78 us at 512 rows x 151936 with one
@@ -373,8 +405,10 @@ cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32
     const int small_split = (V + kSmallCols - 1) / kSmallCols;
     if (vec4 && static_cast<long long>(R) * small_split <= 8ll * sms && small_split <= max_splits_for(R)) {
         *n_split_out = small_split;
+        *merged = fin.row_done != nullptr;
         return launch_dependent(logits_topk_small_kernel<KP>, dim3(static_cast<unsigned>(R), small_split),
-                                dim3(kThreads), 0, stream, logits, V, small_split, pval, pid);
+                                dim3(kThreads), 0, stream, logits, V, small_split, pval, pid, fin.row_done, fin.k,
+                                fin.ids, fin.vals);
     }
     int n_split = std::max(1, (sms + R - 1) / R);
     n_split = std::min({n_split, max_splits_for(R), std::max(1, V / 2048)});
@@ -390,15 +424,20 @@ cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32
 }  // namespace
 
 cudaError_t launch_logits_topk_partial(const float *logits, int R, int V, int KP, float *pval, int32_t *pid,
-                                       int *n_split_out, cudaStream_t stream)
+                                       int *n_split_out, cudaStream_t stream, const TopkFinish &fin, bool *merged)
 {
+    bool m = false;
+    cudaError_t e;
     switch (KP) {
-    case 4: return launch_partial<4>(logits, R, V, pval, pid, n_split_out, stream);
-    case 8: return launch_partial<8>(logits, R, V, pval, pid, n_split_out, stream);
-    case 16: return launch_partial<16>(logits, R, V, pval, pid, n_split_out, stream);
-    case 32: return launch_partial<32>(logits, R, V, pval, pid, n_split_out, stream);
-    default: return cudaErrorInvalidValue;
+    case 4: e = launch_partial<4>(logits, R, V, pval, pid, n_split_out, fin, &m, stream); break;
+    case 8: e = launch_partial<8>(logits, R, V, pval, pid, n_split_out, fin, &m, stream); break;
+    case 16: e = launch_partial<16>(logits, R, V, pval, pid, n_split_out, fin, &m, stream); break;
+    case 32: e = launch_partial<32>(logits, R, V, pval, pid, n_split_out, fin, &m, stream); break;
+    default: e = cudaErrorInvalidValue;
     }
+    if (merged)
+        *merged = m;
+    return e;
 }
 
 cudaError_t launch_topk_merge(const float *pval, const int32_t *pid, int R, int n_split, int KP, int k,

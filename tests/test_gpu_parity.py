@@ -307,6 +307,27 @@ def test_topk_stage_is_exact(R, V, k):
     assert np.array_equal(host(vals).view(np.uint32), o_vals.view(np.uint32))
 
 
+@pytest.mark.parametrize("R,V,k", [(16, 151936, 8), (3, 4096, 4), (64, 262144, 16), (7, 4099, 32), (300, 20000, 16)])
+def test_topk_calls_on_one_workspace_leave_it_clean(R, V, k):
+    """Few rows: the slice kernel's last CTA of each row merges it, counting the row's slices in
+    the workspace's control block; every call returns the counters to zero, so back-to-back calls
+    on one workspace and new logits stay exact (more rows: slice lists and a merge launch)."""
+    rng = np.random.default_rng(R + V + k)
+    ws = df.Workspace(df.make_dims(R, 1, 8, V, k, 8))
+    n_ctrl = _control_bytes(R, 1, k)
+    outs, wants = [], []
+    for c in range(3):
+        lg = rng.standard_normal((R, V)).astype(np.float32)
+        lg[:, 7 % V] = lg[:, 3 % V]
+        wants.append(oracle.topk(lg, k))
+        outs.append(df.dflash2_topk(dev(lg), k, workspace=ws))  # enqueued back to back
+    torch.cuda.synchronize()
+    assert not ws.view[:n_ctrl].any().item(), "control block not zero after the calls"
+    for (ids, vals), (o_ids, o_vals) in zip(outs, wants):
+        assert np.array_equal(host(ids), o_ids)
+        assert np.array_equal(host(vals).view(np.uint32), o_vals.view(np.uint32))
+
+
 @pytest.mark.parametrize("R,V,k,kind", [(4, 8192, 16, "constant"), (3, 12300, 32, "two_levels"), (2, 4096, 4, "constant"),
                                         (5, 20000, 8, "coarse")])
 def test_topk_stage_ties_in_small_slices(R, V, k, kind):
