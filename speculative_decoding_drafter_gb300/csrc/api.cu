@@ -7,10 +7,22 @@
 #include <cstdint>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dflash2.h"
 #include "internal.h"
 
 namespace df2 {
+
+// NVTX range around an entry point: the calls show up by name in a profiler's timeline, and
+// `ncu --nvtx --nvtx-include "dflash2_select/"` captures the kernels of one call.  Without a
+// profiler attached the push and pop return at once (header-only NVTX, no library linked).
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
 
 int device_sm_count()
 {
@@ -297,6 +309,7 @@ df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *
                           int32_t *draft_ids, int32_t *topk_ids, float *topk_logits, float *gate,
                           void *workspace, size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_select");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!hidden || !W_vocab || !aligned(hidden, 16) || !aligned(W_vocab, 16))
@@ -313,6 +326,7 @@ df2_status dflash2_select_walk(const df2_dims *dims, const df2_walk_opts *walk, 
                                const int32_t *anchor, float *lattice, int32_t *draft_ids, int32_t *topk_ids,
                                float *topk_logits, float *gate, void *workspace, size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_select_walk");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     WalkOpts opts;
@@ -338,6 +352,7 @@ df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_host, co
                                float *lattice_host, int32_t *draft_ids_host, uint32_t *status_host, void *workspace,
                                size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_select_host");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!hidden_host || !anchor_host || !draft_ids_host || !W_vocab || !aligned(W_vocab, 16))
@@ -407,6 +422,7 @@ df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits,
                                       int32_t *topk_ids, float *topk_logits, float *gate, void *workspace,
                                       size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_select_from_logits");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!logits || !hidden || !aligned(logits, 16) || !aligned(hidden, 16))
@@ -430,6 +446,7 @@ df2_status dflash2_select_from_logits(const df2_dims *dims, const float *logits,
 df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidden, const void *W_vocab, float *logits,
                                   void *workspace, size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_lm_head_logits");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!hidden || !W_vocab || !logits || !aligned(hidden, 16) || !aligned(W_vocab, 16) || !aligned(logits, 4))
@@ -445,6 +462,7 @@ df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidden, cons
 df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk_ids, float *topk_logits,
                         void *workspace, size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_topk");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!logits || !topk_ids || !topk_logits || !aligned(logits, 16) || !aligned(topk_ids, 4) ||
@@ -473,6 +491,7 @@ df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk
 df2_status dflash2_gate(const df2_dims *dims, const void *hidden, const void *W_sel, float *gate, void *workspace,
                         size_t workspace_bytes, void *stream)
 {
+    const TraceRange range("dflash2_gate");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!hidden || !W_sel || !gate || !aligned(hidden, 16) || !aligned(W_sel, 16) || !aligned(gate, 16))
@@ -489,6 +508,7 @@ df2_status dflash2_lattice(const df2_dims *dims, const int32_t *topk_ids, const 
                            const float *gate, const void *pred_cb, const void *succ_cb, const int32_t *anchor,
                            float *lattice, void *stream)
 {
+    const TraceRange range("dflash2_lattice");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!topk_ids || !topk_logits || !gate || !pred_cb || !succ_cb || !anchor || !lattice)
@@ -505,6 +525,7 @@ df2_status dflash2_lattice(const df2_dims *dims, const int32_t *topk_ids, const 
 
 df2_status dflash2_walk(const df2_dims *dims, const float *lattice, int32_t *draft_ids, void *stream)
 {
+    const TraceRange range("dflash2_walk");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!lattice || !draft_ids || !aligned(lattice, 4) || !aligned(draft_ids, 4))
@@ -518,6 +539,7 @@ df2_status dflash2_walk_sample(const df2_dims *dims, const float *lattice, float
                                const float *uniforms, int32_t *draft_ids, int32_t *n_draft, float *confidence,
                                void *stream)
 {
+    const TraceRange range("dflash2_walk_sample");
     DF2_TRY(check_dims(dims));
     const df2_dims d = *dims;
     if (!lattice || !draft_ids || !aligned(lattice, 4) || !aligned(draft_ids, 4) ||
@@ -535,6 +557,7 @@ df2_status dflash2_walk_sample(const df2_dims *dims, const float *lattice, float
 df2_status dflash2_dynamic_conv(const df2_conv_dims *dims, const void *x, const void *x_prev, const void *base,
                                 const float *dyn, const void *gamma, float eps, void *y, void *stream)
 {
+    const TraceRange range("dflash2_dynamic_conv");
     if (!dims)
         return DF2_ERR_INVALID_ARG;
     const df2_conv_dims d = *dims;
