@@ -17,7 +17,7 @@
 int main(void)
 {
     df2_dims d = {1, 16, 4096, 151936, 8, 256};
-    CHECK(dflash2_version() >= 100);
+    CHECK(dflash2_version() >= 300);
     CHECK(strcmp(dflash2_status_string(DF2_OK), "ok") == 0);
     CHECK(strlen(dflash2_status_string(DF2_ERR_TIMEOUT)) > 2);
 
@@ -37,6 +37,13 @@ int main(void)
                          (void *)(uintptr_t)0x100000, ws, NULL) == DF2_ERR_UNSUPPORTED);
     CHECK(dflash2_select(&d, p, p, p, p, p, (const int32_t *)p, (float *)p, (int32_t *)p, NULL, NULL, NULL,
                          (void *)(uintptr_t)0x100000, ws - 256, NULL) == DF2_ERR_WORKSPACE);
+    /* the walk options are checked before anything else of the call */
+    df2_walk_opts w = {0.0f, 0.5f, NULL, NULL, NULL};
+    CHECK(dflash2_select_walk(&d, &w, p, p, p, p, p, (const int32_t *)p, (float *)p, (int32_t *)p, NULL, NULL, NULL,
+                              (void *)(uintptr_t)0x100000, ws, NULL) == DF2_ERR_INVALID_ARG);
+    w.temperature = 1.0f;
+    CHECK(dflash2_select_walk(&d, &w, p, p, p, p, p, (const int32_t *)p, (float *)p, (int32_t *)p, NULL, NULL, NULL,
+                              (void *)(uintptr_t)0x100000, ws - 256, NULL) == DF2_ERR_WORKSPACE);
     CHECK(dflash2_selftest_wait_timeout(0, (void *)(uintptr_t)0x100000, ws, NULL) == DF2_ERR_INVALID_ARG);
     CHECK(dflash2_profile_events(p, NULL) == DF2_ERR_INVALID_ARG);
     printf("ok\n");
