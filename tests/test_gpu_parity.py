@@ -432,6 +432,21 @@ def test_select_edge_shapes(B, T, H, V, k, D):
     assert compared + low >= 1
 
 
+@pytest.mark.parametrize("B,T,H,V,k,D", [(3, 5, 64, 3000, 16, 1024), (2, 7, 128, 2000, 12, 264), (4, 3, 64, 1500, 9, 8),
+                                         (1, 1, 64, 100, 16, 520), (5, 4, 256, 4000, 13, 256)])
+def test_select_small_cta_finish_shapes(B, T, H, V, k, D):
+    """9 to 16 candidates run the two-warp finish kernel, which stages the codebook rows in passes
+    of at most 256 elements of D: one pass, several, a short last pass, D = 8 (one warp's step)."""
+    cfg, x = small_case(B, T, H, V, k, D, seed=B * T + k + D)
+    lat, draft, vals = run_select(x, cfg)
+    ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
+    tol = row_tol(ora["logits"])
+    ids = lat[:, :k].astype(np.int32)
+    check_fused_candidates(ids, vals, ora["logits"], ora["topk_ids"], ora["topk_vals"], tol)
+    compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
+    assert compared + low >= 1
+
+
 def test_select_largest_vocabulary():
     """V = 2^24 - 1, the largest vocabulary whose ids are exact in the float32 lattice, with k = 32."""
     B, T, H, V, k, D = 1, 2, 8, (1 << 24) - 1, 32, 8
