@@ -437,16 +437,14 @@ __global__ void __launch_bounds__(kTileThreads) finish_tile_kernel(const FinishA
 }
 
 constexpr size_t kWalkSmemCap = 64 * 1024;
-// Fair-share sizing of the finish kernels' shared memory (GB300: 228 KB per SM with the largest
-// carveout, 1 KB reserved per CTA, the kernels' static arrays; the CTAs per SM their registers
-// and shared memory allow anyway).
+// Fair-share sizing of the small-CTA kernel's shared memory (GB300: 228 KB per SM with the
+// largest carveout, 1 KB reserved per CTA, the kernel's static arrays; the CTAs per SM its
+// registers and shared memory allow anyway).
 constexpr size_t kSmemPerSm = 228 * 1024;
 constexpr size_t kSmemReservePerCta = 1024;
 constexpr size_t kTileStaticSmem = 3200;
-constexpr size_t kFinishStaticSmem = 1024;
 constexpr size_t kFairSmemCap = 200 * 1024;
 constexpr long long kTileCtasPerSm = 9;
-constexpr long long kFinishCtasPerSm = 5;
 
 template <int KP>
 cudaError_t launch_kp(FinishArgs a, int B, cudaStream_t stream)
@@ -460,19 +458,18 @@ cudaError_t launch_kp(FinishArgs a, int B, cudaStream_t stream)
     if (a.walk_in_smem && walk_bytes > smem)
         smem = walk_bytes;
     // Launched as a programmatic dependent, the CTAs become resident on the SMs the LM head frees
-    // first and wait there for its grid: up to nine small CTAs (five of 128 threads) on one SM,
-    // so at 512 positions they would crowd onto some 57 SMs.  Shared memory sized to an SM's fair
-    // share of the positions keeps any SM from taking more than ceil(R / SMs) of them.  Measured on
-    // GB300 (same-box A/Bs, interleaved): from the LM head to the end of the step 23.3 -> 15.7 us
-    // at 512 rows with the small CTAs (18.9 with the 128-thread kernel); the finish kernel alone
-    // 14.4 -> 13.9 us at 16 rows and 13.6 -> 12.8 us at 64.
-    {
+    // first and wait there for its grid: up to nine small CTAs on one SM, so at 512 positions
+    // they would crowd onto some 57 SMs.  Shared memory sized to an SM's fair share of the
+    // positions keeps any SM from taking more than ceil(R / SMs) of them.  Measured on GB300
+    // (same-box A/Bs, interleaved): from the LM head to the end of the step 23.3 -> 15.7 us at 512
+    // rows (18.9 with the 128-thread kernel).  The same sizing did nothing for the 128-thread
+    // kernel at 16 and 64 rows (14.19 against 14.17 us for the kernel alone), so it keeps its own.
+    if (tile) {
         const long long R = static_cast<long long>(B) * a.T;
         const long long sms = device_sm_count();
         const long long share = (R + sms - 1) / sms;
-        if (share < (tile ? kTileCtasPerSm : kFinishCtasPerSm)) {
-            size_t want = kSmemPerSm / static_cast<size_t>(share) - kSmemReservePerCta -
-                          (tile ? kTileStaticSmem : kFinishStaticSmem);
+        if (share < kTileCtasPerSm) {
+            size_t want = kSmemPerSm / static_cast<size_t>(share) - kSmemReservePerCta - kTileStaticSmem;
             if (want > kFairSmemCap)
                 want = kFairSmemCap;
             if (want > smem)
@@ -482,7 +479,7 @@ cudaError_t launch_kp(FinishArgs a, int B, cudaStream_t stream)
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), static_cast<int>(smem));
     if (e != cudaSuccess)
         return e;
-    {
+    if (tile) {
         // as much shared memory as the SM has (the fair-share sizing above counts on it)
         thread_local int carveout_set_for = -1;
         int dev = 0;
