@@ -191,6 +191,9 @@ __device__ __forceinline__ void walk_if_last(const FinishArgs &a, int b, long lo
         a.counters[b] = 0u;
 }
 
+// The merge and the walk are written out here rather than through the device functions
+// above, which the small-CTA kernel uses: the same code through them ran 1.1-1.5 us slower at
+// 16 and 64 rows in a same-box A/B (identical outputs).
 template <int KP>
 __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs a)
 {
@@ -216,16 +219,82 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
         *a.status_mirror = *reinterpret_cast<const volatile uint32_t *>(a.status);
 
     const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int k = a.k;
 
     // ---- 1. merge (warp 0: row r, warp 1: row r-1) while the other warps fetch the gate row
-    if (warp == 0)
-        merge_row_lists<KP>(a, r, s_cand, s_unary, s_mv[0], s_mi[0]);
-    else if (warp == 1 && t > 0)
-        merge_row_lists<KP>(a, r - 1, s_prev, nullptr, s_mv[1], s_mi[1]);
-    else if (warp >= 2)
+    if (warp < 2 && (warp == 0 || t > 0)) {
+        const long long row_base = static_cast<long long>(warp == 0 ? r : r - 1) * a.n_split * KP;
+        float av[KP];
+        int ai[KP];
+#pragma unroll
+        for (int s = 0; s < KP; ++s) {
+            av[s] = -INFINITY;
+            ai[s] = INT_MAX;
+        }
+        // several lists per lane per round, all loads issued before the merges
+        constexpr int kLists = KP <= 8 ? 5 : KP <= 16 ? 2 : 1;
+        for (int list0 = lane; list0 < a.n_split; list0 += 32 * kLists) {
+            float bv[kLists][KP];
+            int bi[kLists][KP];
+#pragma unroll
+            for (int u = 0; u < kLists; ++u) {
+                const int list = list0 + 32 * u;
+                const bool have = list < a.n_split;
+                const long long off = row_base + static_cast<long long>(have ? list : 0) * KP;
+                const float4 *pv = reinterpret_cast<const float4 *>(a.pval + off);
+                const int4 *pi = reinterpret_cast<const int4 *>(a.pid + off);
+#pragma unroll
+                for (int q = 0; q < KP / 4; ++q) {
+                    const float4 v4 = __ldcg(pv + q);
+                    const int4 i4 = __ldcg(pi + q);
+                    bv[u][4 * q] = have ? v4.x : -INFINITY;
+                    bv[u][4 * q + 1] = have ? v4.y : -INFINITY;
+                    bv[u][4 * q + 2] = have ? v4.z : -INFINITY;
+                    bv[u][4 * q + 3] = have ? v4.w : -INFINITY;
+                    bi[u][4 * q] = have ? i4.x : INT_MAX;
+                    bi[u][4 * q + 1] = have ? i4.y : INT_MAX;
+                    bi[u][4 * q + 2] = have ? i4.z : INT_MAX;
+                    bi[u][4 * q + 3] = have ? i4.w : INT_MAX;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kLists; ++u)
+                merge_top<KP>(av, ai, bv[u], bi[u]);
+        }
+        // the lanes' lists into the row's top-k: the bounded merge (measured on GB300 at 512
+        // rows, k = 16: far fewer instructions than the butterfly), else the butterfly
+        float mv;
+        int mi;
+        if (KP <= 16 && bounded_merge<KP>(av, ai, s_mv[warp], s_mi[warp], mv, mi)) {
+            if (lane < k) {
+                if (warp == 0) {
+                    s_cand[lane] = clamp_id(mi, a.V);
+                    s_unary[lane] = mv;
+                } else {
+                    s_prev[lane] = clamp_id(mi, a.V);
+                }
+            }
+        } else {
+            warp_merge_top<KP>(av, ai, 31);
+            if (lane == 0) {
+#pragma unroll
+                for (int s = 0; s < KP; ++s) {
+                    if (s < k) {
+                        if (warp == 0) {
+                            s_cand[s] = clamp_id(ai[s], a.V);
+                            s_unary[s] = av[s];
+                        } else {
+                            s_prev[s] = clamp_id(ai[s], a.V);
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp >= 2) {
         load_gate_row(reinterpret_cast<float *>(smem), a.gate + static_cast<long long>(r) * a.D, a.D, 64,
                       blockDim.x - 64);
+    }
     if (t == 0 && threadIdx.x == 0)
         s_prev[0] = clamp_id(anchor_b, a.V);
     __syncthreads();
@@ -237,14 +306,63 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishArgs
             a.topk_vals[o] = s_unary[threadIdx.x];
     }
 
-// ---- 2. lattice row and the walk's choice from each predecessor row
+    // ---- 2. lattice row and the walk's choice from each predecessor row
     const long long width = k + static_cast<long long>(k) * k;
     lattice_row<KP>(k, a.D, t == 0 ? 1 : k, s_prev, s_cand, s_unary, a.pred_cb, a.succ_cb, smem,
                     a.lattice + r * width, a.best + static_cast<long long>(r) * k,
                     a.lattice_mirror ? a.lattice_mirror + r * width : nullptr);
 
     // ---- 3. the last CTA of the sequence walks it
-    walk_if_last(a, b, width, smem, &s_last);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = atomicAdd(a.counters + b, 1u) == static_cast<unsigned>(a.T - 1);
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    const long long r0 = static_cast<long long>(b) * a.T;
+    const int32_t *best = a.best + r0 * k;
+    const float *rows = a.lattice + r0 * width;
+    int32_t *draft = a.draft + r0;
+    int32_t *draft_mirror = a.draft_mirror ? a.draft_mirror + r0 : nullptr;
+    if (a.sample_walk) {
+        // the confidence of each step needs the whole row the walk reads: one warp walks the
+        // rows through L2, with the same device code as the stand-alone sampling walk
+        if (warp == 0)
+            walk_sample_rows<true>(a.T, k, width, rows, a.temperature, a.p_min, a.uniforms ? a.uniforms + r0 : nullptr,
+                                   draft, draft_mirror, a.n_draft ? a.n_draft + b : nullptr,
+                                   a.confidence ? a.confidence + r0 : nullptr);
+    } else if (a.walk_in_smem) {
+        int *sb = reinterpret_cast<int *>(smem);     // [T][k] choices
+        int *sid = sb + a.T * k;                     // [T][k] candidate ids
+        for (int i = threadIdx.x; i < a.T * k; i += blockDim.x) {
+            const int tt = i / k, j = i - tt * k;
+            sb[i] = __ldcg(best + i);
+            sid[i] = static_cast<int>(__ldcg(rows + tt * width + j));
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int j = 0;
+            for (int tt = 0; tt < a.T; ++tt) {
+                j = sb[tt * k + j];
+                draft[tt] = sid[tt * k + j];
+                if (draft_mirror)
+                    draft_mirror[tt] = sid[tt * k + j];
+            }
+        }
+    } else if (threadIdx.x == 0) {
+        int j = 0;
+        for (int tt = 0; tt < a.T; ++tt) {
+            j = __ldcg(best + static_cast<long long>(tt) * k + j);
+            const int32_t id = static_cast<int32_t>(__ldcg(rows + tt * width + j));
+            draft[tt] = id;
+            if (draft_mirror)
+                draft_mirror[tt] = id;
+        }
+    }
+    if (threadIdx.x == 0)
+        a.counters[b] = 0u;
 }
 
 // ---------------------------------------------------------------- 9 to 16 candidates: small CTAs
@@ -318,10 +436,9 @@ __global__ void __launch_bounds__(kTileThreads) finish_tile_kernel(const FinishA
     const float *grow = a.gate + static_cast<long long>(r) * D;
     for (int i = threadIdx.x; i < D / 4; i += kTileThreads)
         cp_async_16(sg + 4 * i, grow + 4 * i);
-    if (warp == 0)
-        merge_row_lists<KP>(a, r, s_cand, s_unary, s_mv[0], s_mi[0]);
-    else if (t > 0)
-        merge_row_lists<KP>(a, r - 1, s_prev, nullptr, s_mv[1], s_mi[1]);
+    if (warp == 0 || t > 0)
+        merge_row_lists<KP>(a, warp == 0 ? r : r - 1, warp == 0 ? s_cand : s_prev, warp == 0 ? s_unary : nullptr,
+                            s_mv[warp], s_mi[warp]);
     __syncthreads();
     if (t == 0 && threadIdx.x < k)
         s_prev[threadIdx.x] = s_anchor;
