@@ -222,8 +222,8 @@ __device__ __forceinline__ void merge_row_lists(const float *pval, const int32_t
     }
 }
 
-// Few rows (a grid of one wave): one CTA per (row, 4096-column slice), a
-// thread holding 16 values in registers.  The per-warp list of the kernel above spends most of
+// Few rows (a grid of about one wave): one CTA per (row, balanced slice of at most 5120 columns),
+// a thread holding 20 values in registers.  The per-warp list of the kernel above spends most of
 // its time in the chain of insertions while a list fills, which at 16 rows is the whole
 // kernel; here no list is filled value by value.  Warp w takes tau_w, the ceil(KP / 8)-th
 // largest of its lanes' maxima: at least ceil(KP / 8) values of distinct columns are at or
@@ -234,13 +234,11 @@ __device__ __forceinline__ void merge_row_lists(const float *pval, const int32_t
 // With row_done (one counter per row, zero before the launch and zero again after it) the
 // kernel also finishes the rows: the CTA that completes a row's last slice, found by an atomic
 // counter (nothing waits), merges the row's slice lists into ids / vals, so no merge launch
-// follows.  Measured on GB300 by CUDA-graph replay, identical outputs: 13.0 us per call at 16
-// rows x 151936 (k = 8), as with a separate merge launch (12.98 us), which the programmatic
-// dependent launch already overlapped.  What sets the time is a chain of dependent latencies
-// (instrumented copy): the slice CTAs end 9 us after the first starts (each works about 6.7k
-// cycles: loads, the lane-maximum sort, the survivors' sort), then the row's last CTA counts
-// and merges 38 lists (about 7k cycles).
-constexpr int kSmallPerThread = 16;                          // values per thread
+// follows.  Measured on GB300 by CUDA-graph replay, identical outputs, at 16 rows x 151936
+// (k = 8): as fast as a separate merge launch, which the programmatic dependent launch already
+// overlapped (13.0 against 12.98 us with the earlier slicing); the balanced slices below took it
+// to 8.0 us.
+constexpr int kSmallPerThread = 20;                          // values per thread (5120 columns per CTA)
 constexpr int kSmallCols = kThreads * kSmallPerThread;       // columns per CTA
 
 template <int KP>
@@ -262,8 +260,16 @@ __global__ void __launch_bounds__(kThreads) logits_topk_small_kernel(const float
     const int s = blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int c0 = s * kSmallCols;           // first column of the slice (V is a multiple of 4)
-    const int c1 = min(V, c0 + kSmallCols);
+    // Balanced slices: the row's V / 4 groups of four columns split evenly (at most
+    // ceil(V / 4 / n_split) <= kSmallCols / 4 groups each; V is a multiple of 4).  Slices of
+    // kSmallCols with a short remainder left the last one a few hundred columns, most of its
+    // warps empty, their bound -inf and every value a survivor: each row then waited for that
+    // CTA's sorts.  Measured on GB300 by CUDA-graph replay, identical outputs: 13.0 -> 9.2 us per
+    // call at 16 x 151936 with balanced slices of 4096 columns at most, 8.0 with 5120 (30 slices
+    // instead of 38); 12.98 -> 12.37 us at 16 x 262144.
+    const int groups = V / 4;
+    const int c0 = static_cast<int>(static_cast<long long>(s) * groups / n_split) * 4;
+    const int c1 = static_cast<int>(static_cast<long long>(s + 1) * groups / n_split) * 4;
     const float4 *row4 = reinterpret_cast<const float4 *>(logits + static_cast<long long>(r) * V);
     if (threadIdx.x == 0)
         s_count = 0;
@@ -409,9 +415,10 @@ cudaError_t launch_partial(const float *logits, int R, int V, float *pval, int32
     // slice per row, 95 us with two, 139 us with four).
     const bool vec4 = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15u) == 0);
     const int sms = device_sm_count();
-    // Few rows: slices of 4096 columns without per-warp lists, while the grid fits one wave
-    // (measured on GB300, same ids and values: 28.3 -> 26.3 us per call at 16 x 151936, 40.6 ->
-    // 35.6 at 16 x 262144; 32.4 -> 38.6 at 64 x 152064, 2432 CTAs, so larger grids keep the lists)
+    // Few rows: slices of at most 5120 columns without per-warp lists, while the grid is small
+    // (measured on GB300 with 4096-column slices, same ids and values: 28.3 -> 26.3 us per call
+    // at 16 x 151936, 40.6 -> 35.6 at 16 x 262144; 32.4 -> 38.6 at 64 x 152064, 2432 CTAs, so
+    // larger grids keep the lists)
     const int small_split = (V + kSmallCols - 1) / kSmallCols;
     if (vec4 && static_cast<long long>(R) * small_split <= 8ll * sms && small_split <= max_splits_for(R)) {
         *n_split_out = small_split;
