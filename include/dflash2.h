@@ -116,8 +116,8 @@ DF2_API df2_status dflash2_workspace_init(const df2_dims *dims, void *workspace,
  *   topk_ids int32 [B*T, k], topk_logits float [B*T, k], gate float [B*T, D]:
  *            optional copies of the candidates (sorted by logit desc, id asc), their
  *            logits (the unary scores) and the gate; NULL to skip.
- * Two launches: the tensor-core LM head (which also computes the gate) and one kernel
- * for the merge, lattice and walk.  The full float32 logits never reach global memory:
+ * Two launches: the tensor-core LM head (which also computes the gate; CTA pairs with
+ * tcgen05.mma.cta_group::2 from 129 to 1024 rows) and one kernel for the merge, lattice and walk.  The full float32 logits never reach global memory:
  * each CTA of the LM head keeps a per-row top-k of its vocabulary slice in registers.
  */
 DF2_API df2_status dflash2_select(const df2_dims *dims, const void *hidden, const void *W_vocab, const void *W_sel,
@@ -198,7 +198,9 @@ DF2_API df2_status dflash2_select_host(const df2_dims *dims, const void *hidden_
                                        const int32_t *anchor_host, float *lattice_host, int32_t *draft_ids_host,
                                        uint32_t *status_host, void *workspace, size_t workspace_bytes, void *stream);
 
-/* ---- single steps of the path (same kernels as above), for stage-by-stage checks ---- */
+/* ---- single steps of the path (the device code of the calls above), for stage-by-stage checks.
+ * dflash2_lattice scores in the 128-thread layout; for 9 to 16 candidates dflash2_select scores
+ * in two-warp CTAs, so its lattice sums in another order (both within the float32 bound). ---- */
 
 /* LM head alone: logits float [B*T, V] = hidden . W_vocab^T with float32 accumulation
  * (tensor cores, same main loop as dflash2_select; this variant stores the tile instead
@@ -207,7 +209,9 @@ DF2_API df2_status dflash2_lm_head_logits(const df2_dims *dims, const void *hidd
                                   void *workspace, size_t workspace_bytes, void *stream);
 
 /* Top-k of given float32 logits [B*T, V]: topk_ids int32 [B*T, k], topk_logits float [B*T, k],
- * ordered by (logit desc, id asc).  "DFlash2 Lands in llama.cpp", candidates = top_k(logits). */
+ * ordered by (logit desc, id asc).  "DFlash2 Lands in llama.cpp", candidates = top_k(logits).
+ * At few rows one launch: the CTA that completes a row's last column slice merges the row,
+ * counting slices in the workspace's control block (left at zero, like every call). */
 DF2_API df2_status dflash2_topk(const df2_dims *dims, const float *logits, int32_t *topk_ids, float *topk_logits,
                         void *workspace, size_t workspace_bytes, void *stream);
 
