@@ -433,10 +433,12 @@ def test_select_edge_shapes(B, T, H, V, k, D):
 
 
 @pytest.mark.parametrize("B,T,H,V,k,D", [(3, 5, 64, 3000, 16, 1024), (2, 7, 128, 2000, 12, 264), (4, 3, 64, 1500, 9, 8),
-                                         (1, 1, 64, 100, 16, 520), (5, 4, 256, 4000, 13, 256)])
+                                         (1, 1, 64, 100, 16, 520), (5, 4, 256, 4000, 13, 256),
+                                         (2, 300, 64, 5000, 16, 64), (1, 700, 64, 3000, 15, 32)])
 def test_select_small_cta_finish_shapes(B, T, H, V, k, D):
     """9 to 16 candidates run the two-warp finish kernel, which stages the codebook rows in passes
-    of at most 256 elements of D: one pass, several, a short last pass, D = 8 (one warp's step)."""
+    of at most 256 elements of D: one pass, several, a short last pass, D = 8 (one warp's step);
+    long sequences walk from shared memory (T*k*8 bytes up to 64 KB) or from global memory."""
     cfg, x = small_case(B, T, H, V, k, D, seed=B * T + k + D)
     lat, draft, vals = run_select(x, cfg)
     ora = oracle.select(x["hidden"], x["W_vocab"], x["W_sel"], x["pred_cb"], x["succ_cb"], x["anchor"], k, T)
@@ -445,6 +447,13 @@ def test_select_small_cta_finish_shapes(B, T, H, V, k, D):
     check_fused_candidates(ids, vals, ora["logits"], ora["topk_ids"], ora["topk_vals"], tol)
     compared, low = compare_lattice_and_draft(lat, draft, ora, T, k, tol)
     assert compared + low >= 1
+    # the walk follows the lattice the kernel wrote, step by step, whatever the oracle's margins
+    for b in range(B):
+        j = 0
+        for t in range(T):
+            row = lat[b * T + t]
+            j = int(np.argmax(row[k + j * k:k + (j + 1) * k]))  # first maximum
+            assert draft[b, t] == int(row[j]), f"sequence {b} position {t}"
 
 
 def test_select_largest_vocabulary():
