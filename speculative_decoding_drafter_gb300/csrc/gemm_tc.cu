@@ -50,8 +50,10 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cfloat>
 #include <cstdint>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -595,18 +597,59 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
     }
 }
 
+// The driver's encoder, looked up on first use (again after a failed lookup); safe to call from
+// several host threads.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+    PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
     if (!fn) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q{};
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+            q == cudaDriverEntryPointSuccess) {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+            cached.store(fn, std::memory_order_release);
+        }
     }
     return fn;
+}
+
+// CTAs of a pair kernel resident at once on the current device (clusters of two need two SMs
+// of one GPC), cached per device and KP instantiation (kp_slot); safe to call from several
+// host threads.
+int resident_pair_ctas(const void *kern, int kp_slot, int smem_bytes, int sms)
+{
+    static std::mutex mu;
+    static int cache[64][4] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return std::max(2, sms / 2 * 2);
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    int &cached = cache[dev][kp_slot];
+    if (cached == 0) {
+        cudaLaunchConfig_t qc = {};
+        qc.gridDim = dim3(static_cast<unsigned>(2 * sms));
+        qc.blockDim = dim3(64 + BM);
+        qc.dynamicSmemBytes = smem_bytes;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        qc.attrs = qa;
+        qc.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &qc) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();
+            clusters = sms / 2;
+        }
+        cached = std::min(sms, 2 * clusters);
+    }
+    return cached;
 }
 
 // Row-major bf16 [rows, K] tensor, boxes of 64 K-elements x box_rows rows, 128-byte swizzle.
@@ -760,31 +803,9 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
         args.group_done = nullptr;
     }
     int ctas = sms;  // CTAs resident at once: one per SM
-    if (args.pair) {
-        // pairs need two SMs of one GPC: size the grid by the pairs that fit at once
-        static int pair_ctas[4] = {0, 0, 0, 0};  // per KP instantiation
-        int &cached = pair_ctas[KP == 4 ? 0 : KP == 8 ? 1 : KP == 16 ? 2 : 3];
-        if (cached == 0) {
-            cudaLaunchConfig_t qc = {};
-            qc.gridDim = dim3(static_cast<unsigned>(2 * sms));
-            qc.blockDim = dim3(64 + BM);
-            qc.dynamicSmemBytes = smem_bytes;
-            cudaLaunchAttribute qa[1];
-            qa[0].id = cudaLaunchAttributeClusterDimension;
-            qa[0].val.clusterDim.x = 2;
-            qa[0].val.clusterDim.y = 1;
-            qa[0].val.clusterDim.z = 1;
-            qc.attrs = qa;
-            qc.numAttrs = 1;
-            int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, kern, &qc) != cudaSuccess || clusters < 1) {
-                (void)cudaGetLastError();
-                clusters = sms / 2;
-            }
-            cached = std::min(sms, 2 * clusters);
-        }
-        ctas = cached;
-    }
+    if (args.pair)  // pairs need two SMs of one GPC: size the grid by the pairs that fit at once
+        ctas = resident_pair_ctas(reinterpret_cast<const void *>(kern), KP == 4 ? 0 : KP == 8 ? 1 : KP == 16 ? 2 : 3,
+                                  smem_bytes, sms);
     args.n_split = std::max(1, std::min({max_splits_for(R), units, std::max(1, ctas / args.row_groups)}));
     if (n_split_out)
         *n_split_out = args.n_split;

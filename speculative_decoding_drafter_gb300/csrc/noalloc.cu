@@ -10,6 +10,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -43,13 +44,17 @@ int g_scratch_used = 0;
 CUcontext current_context()
 {
     using GetCurrent = CUresult (*)(CUcontext *);
-    static GetCurrent fn = nullptr;
+    // looked up on first use (again after a failed lookup); safe from several host threads
+    static std::atomic<GetCurrent> cached{nullptr};
+    GetCurrent fn = cached.load(std::memory_order_acquire);
     if (!fn) {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q{};
         if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
+            q == cudaDriverEntryPointSuccess) {
             fn = reinterpret_cast<GetCurrent>(p);
+            cached.store(fn, std::memory_order_release);
+        }
     }
     CUcontext ctx = nullptr;
     if (!fn || fn(&ctx) != CUDA_SUCCESS)
