@@ -201,7 +201,18 @@ __device__ __forceinline__ void merge_row_lists(const float *pval, const int32_t
             bi[4 * q + 2] = i4.z;
             bi[4 * q + 3] = i4.w;
         }
-        merge_top<KP>(av, ai, bv, bi);
+        if (list == lane) {
+            // the lane's first list is sorted in the merge's order already: it is the running
+            // list (measured on GB300 by CUDA-graph replay, identical outputs: 8.04 -> 7.36 us per
+            // call at 16 x 151936 with k = 8, where every lane takes one list of the 30)
+#pragma unroll
+            for (int j = 0; j < KP; ++j) {
+                av[j] = bv[j];
+                ai[j] = bi[j];
+            }
+        } else {
+            merge_top<KP>(av, ai, bv, bi);
+        }
     }
     float mv;
     int mi;
