@@ -280,9 +280,10 @@ __global__ void __launch_bounds__(64 + MT * BM, 1)
             const uint64_t stream_policy = l2_policy_evict_first();
             if (args.dependent) {
                 // The weights do not depend on the grid before this one: bring the first
-                // stages' W boxes into L2 while it finishes, then wait for it before any
-                // load of A (the hidden states may be its output).
-                const int warm = min(kWarmStages, n_chunks * kstages);
+                // stages' W boxes into L2 while it finishes (one tile per CTA only: a pair's
+                // feed is bound by TMA operations), then wait for it before any load of A (the
+                // hidden states may be its output).
+                const int warm = PAIR ? 0 : min(kWarmStages, n_chunks * kstages);
                 for (int n = 0; n < warm; ++n) {
                     const Chunk wch = chunk_of(args, slice, n / kstages);
                     const CUtensorMap *wmap = wch.store ? &map_s_wide : &map_t_wide;
@@ -792,9 +793,12 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     const int units = (args.n_topk_pad + n_store + UNIT - 1) / UNIT;
     // Starting under the grid before and warming L2 with W pays where the W stream sets the
     // time (one tile per CTA; measured on GB300: 205.6 -> 201.1 us per back-to-back call at
-    // 16 rows); with two tiles the feed is bound by TMA operations and the prefetch costs
-    // (1739 -> 1797 us at 1024 rows), so those launches stay plain.
-    if (args.mt != 1 || args.pair)
+    // 16 rows).  CTA pairs start under it too, with no warm-up (their setup and the launch
+    // itself leave the step; measured on GB300, same-box interleaved A/B of 60 rounds, identical
+    // outputs: 420.4 -> 417.1 us per step at 512 rows, the same median at 1024).  Two tiles in
+    // one CTA stay plain: the prefetch cost 1739 -> 1797 us at 1024 rows and the bare dependent
+    // launch 1757 -> 1830.
+    if (args.mt != 1 && !args.pair)
         args.dependent = 0;
     // the shared bound pays where the MMA waits for the epilogue (one accumulator buffer; with
     // pairs, measured on GB300, it cost 7 us at 512 rows)
@@ -819,19 +823,23 @@ cudaError_t launch(const void *A, int R, int K, const void *Bt, int n_topk, cons
     cfg.blockDim = dim3(64 + args.mt * BM);
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    int n_attr = 0;
     if (args.pair) {
         // CTAs 2i and 2i + 1 (row tiles 2j and 2j + 1 of one slice: row_groups is even)
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-    } else {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[n_attr].id = cudaLaunchAttributeClusterDimension;
+        attr[n_attr].val.clusterDim.x = 2;
+        attr[n_attr].val.clusterDim.y = 1;
+        attr[n_attr].val.clusterDim.z = 1;
+        ++n_attr;
+    }
+    if (args.dependent) {
+        attr[n_attr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n_attr].val.programmaticStreamSerializationAllowed = 1;
+        ++n_attr;
     }
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = n_attr;
     if ((e = cudaLaunchKernelEx(&cfg, kern, ma, mtw, mtn, msw, msn, args)) != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -845,7 +853,7 @@ cudaError_t launch_lm_head(const void *hidden, int R, int K, const void *W_vocab
                            bool dependent, cudaStream_t stream)
 {
     GemmArgs a{};
-    a.dependent = dependent ? 1 : 0;  // one-tile launches only, decided in launch()
+    a.dependent = dependent ? 1 : 0;  // one-tile and pair launches only, decided in launch()
     a.pval = pval;
     a.pid = pid;
     a.out = out;

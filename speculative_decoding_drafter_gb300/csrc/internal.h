@@ -37,9 +37,10 @@ cudaError_t ensure_dynamic_smem(const void *kernel, int bytes);
 // as float32 out[r * ldo + n].  V = 0 or n_store = 0 drops that segment.  bound [R, KP] and
 // group_done [lm_head_max_groups(R)] are scratch that is zero before the launch and zero
 // again after it: a lower bound on each row's KP-th best logit that the CTAs share.
-// dependent: launch as a programmatic dependent of the grid before it on the stream; the
-// kernel then brings its first weight boxes into L2 and waits for that grid before it
-// reads hidden or writes anything.
+// dependent: launch as a programmatic dependent of the grid before it on the stream (one
+// row tile per CTA, or CTA pairs); the kernel then sets up (and, with one tile per CTA,
+// brings its first weight boxes into L2) and waits for that grid before it reads hidden or
+// writes anything.
 cudaError_t launch_lm_head(const void *hidden, int R, int K, const void *W_vocab, int V, int KP, float *pval,
                            int32_t *pid, int *n_split_out, const void *W_store, int n_store, float *out,
                            long long ldo, uint32_t *bound, unsigned *group_done, uint32_t *status,
