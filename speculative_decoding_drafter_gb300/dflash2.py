@@ -10,6 +10,7 @@ an error.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -132,6 +133,32 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _torch_stream(stream):
+    """torch's object for a `stream` argument (a torch stream, or an int: a raw handle)."""
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    handle = int(stream)
+    return torch.cuda.default_stream() if handle == 0 else torch.cuda.ExternalStream(handle)
+
+
+def _on_stream(fn):
+    """Runs a wrapper with its `stream` as torch's current stream, so that what it allocates
+    (outputs, a workspace zeroed when allocated) is filled on, and reused in the order of, the
+    stream the library launches on."""
+
+    @functools.wraps(fn)
+    def wrapper(*args, stream=None, **kwargs):
+        if stream is None or not torch.cuda.is_available():
+            # the current stream is the launch stream already (without a GPU the wrapper's
+            # argument checks raise before any CUDA call)
+            return fn(*args, stream=stream, **kwargs)
+        ts = _torch_stream(stream)
+        with torch.cuda.stream(ts):
+            return fn(*args, stream=ts, **kwargs)
+
+    return wrapper
+
+
 def _ptr(t, dtype, shape, name):
     if t is None:
         return None
@@ -159,6 +186,7 @@ def dflash2_workspace_bytes(dims: Dims) -> int:
     return int(library().dflash2_workspace_bytes(ctypes.byref(dims)))
 
 
+@_on_stream
 def dflash2_workspace_init(workspace: "Workspace", stream=None) -> None:
     """Zero the workspace's control block (status word, counters, the LM head's bound slots) on the stream."""
     _check(library().dflash2_workspace_init(ctypes.byref(workspace.dims), workspace.ptr, workspace.nbytes,
@@ -166,7 +194,8 @@ def dflash2_workspace_init(workspace: "Workspace", stream=None) -> None:
 
 
 class Workspace:
-    """Device scratch for one problem size (uint8 tensor, 256-byte aligned, allocated zeroed)."""
+    """Device scratch for one problem size (uint8 tensor, 256-byte aligned, zeroed on the current stream
+    when allocated)."""
 
     def __init__(self, dims: Dims, device=None):
         n = dflash2_workspace_bytes(dims)
@@ -233,6 +262,7 @@ def _dims_of(hidden, W_vocab_or_none, W_sel, pred_cb, k, T, V=None):
     return make_dims(R // T, T, H, V, k, D)
 
 
+@_on_stream
 def dflash2_select(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, lattice=None,
                    draft_ids=None, topk_ids=None, topk_logits=None, gate=None, workspace=None, stream=None):
     """Whole selector head on the GPU. Returns (lattice [B*T, k+k*k] float32, draft_ids [B, T] int32)."""
@@ -254,6 +284,7 @@ def dflash2_select(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: 
     return lattice, draft_ids
 
 
+@_on_stream
 def dflash2_select_walk(hidden, W_vocab, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, temperature: float = 1.0,
                         p_min: float = 0.0, uniforms=None, lattice=None, draft_ids=None, n_draft=None,
                         confidence=None, topk_ids=None, topk_logits=None, gate=None, workspace=None, stream=None):
@@ -311,6 +342,7 @@ def _select_host_args(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host
     return args, keep, lattice_host, draft_ids_host
 
 
+@_on_stream
 def dflash2_select_host(hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k: int, T: int, *,
                         lattice_host=None, draft_ids_host=None, workspace: HostWorkspace | None = None, stream=None):
     """Selector head with host-memory inputs and results (pin them for asynchronous copies).
@@ -333,6 +365,7 @@ class SelectHostPlan:
     The bound tensors are kept alive; write the next step's hidden states and anchors into
     them in place.  Calling returns (lattice_host or None, draft_ids_host)."""
 
+    @_on_stream
     def __init__(self, hidden_host, W_vocab, W_sel, pred_cb, succ_cb, anchor_host, k: int, T: int, *,
                  lattice_host=None, draft_ids_host=None, workspace: HostWorkspace | None = None, stream=None,
                  pinned_status: bool = True):
@@ -350,6 +383,7 @@ class SelectHostPlan:
         return self.lattice_host, self.draft_ids_host
 
 
+@_on_stream
 def dflash2_select_from_logits(logits, hidden, W_sel, pred_cb, succ_cb, anchor, k: int, T: int, *, lattice=None,
                                draft_ids=None, topk_ids=None, topk_logits=None, gate=None, workspace=None,
                                stream=None):
@@ -372,6 +406,7 @@ def dflash2_select_from_logits(logits, hidden, W_sel, pred_cb, succ_cb, anchor, 
     return lattice, draft_ids
 
 
+@_on_stream
 def dflash2_lm_head_logits(hidden, W_vocab, *, out=None, workspace=None, stream=None):
     """float32 logits [R, V] from the tensor-core LM head (stage check / standalone use)."""
     R, H = hidden.shape
@@ -388,6 +423,7 @@ def dflash2_lm_head_logits(hidden, W_vocab, *, out=None, workspace=None, stream=
     return out
 
 
+@_on_stream
 def dflash2_topk(logits, k: int, *, ids=None, vals=None, workspace=None, stream=None):
     """Top-k of float32 logits [R, V] by (value desc, id asc). Returns (ids int32 [R,k], vals float32 [R,k])."""
     R, V = logits.shape
@@ -403,6 +439,7 @@ def dflash2_topk(logits, k: int, *, ids=None, vals=None, workspace=None, stream=
     return ids, vals
 
 
+@_on_stream
 def dflash2_topk_noalloc(logits, k: int, *, ids=None, vals=None, stream=None):
     """dflash2_topk without a workspace (the library's own fixed device array holds the
     scratch); for callers that cannot allocate.  Overlapping calls race."""
@@ -417,6 +454,7 @@ def dflash2_topk_noalloc(logits, k: int, *, ids=None, vals=None, stream=None):
     return ids, vals
 
 
+@_on_stream
 def dflash2_gate(hidden, W_sel, *, out=None, workspace=None, stream=None):
     """Gate float32 [R, D] = hidden . W_sel^T on tensor cores."""
     R, H = hidden.shape
@@ -431,6 +469,7 @@ def dflash2_gate(hidden, W_sel, *, out=None, workspace=None, stream=None):
     return out
 
 
+@_on_stream
 def dflash2_lattice(topk_ids, topk_logits, gate, pred_cb, succ_cb, anchor, T: int, *, out=None, stream=None):
     """Packed lattice [B*T, k+k*k] from candidates, unary scores and the gate."""
     R, k = topk_ids.shape
@@ -450,6 +489,7 @@ def dflash2_lattice(topk_ids, topk_logits, gate, pred_cb, succ_cb, anchor, T: in
     return out
 
 
+@_on_stream
 def dflash2_walk(lattice, B: int, T: int, k: int, *, out=None, stream=None):
     """Greedy walk over packed rows: draft ids int32 [B, T]."""
     d = make_dims(B, T, 8, max(k, 1), k, 8)
@@ -460,6 +500,7 @@ def dflash2_walk(lattice, B: int, T: int, k: int, *, out=None, stream=None):
     return out
 
 
+@_on_stream
 def dflash2_walk_sample(lattice, B: int, T: int, k: int, *, temperature: float = 1.0, p_min: float = 0.0,
                         uniforms=None, draft=None, n_draft=None, confidence=None, stream=None):
     """Walk with confidence and p_min stop; inverse-CDF sampling when ``uniforms`` [B, T] is given.
@@ -480,6 +521,7 @@ def dflash2_walk_sample(lattice, B: int, T: int, k: int, *, temperature: float =
     return draft, n_draft, confidence
 
 
+@_on_stream
 def dflash2_dynamic_conv(x, base, dyn, T: int, *, x_prev=None, gamma=None, eps: float = 1e-6, G: int = 16, out=None,
                          stream=None):
     """Two-tap dynamic depthwise conv of B blocks of T rows: bf16 [B*T, C] -> bf16 [B*T, C]."""
@@ -498,12 +540,14 @@ def dflash2_dynamic_conv(x, base, dyn, T: int, *, x_prev=None, gamma=None, eps: 
     return out
 
 
+@_on_stream
 def dflash2_check_device_status(workspace: Workspace, stream=None) -> None:
     """Synchronises the stream; raises DFlash2Error(DF2_ERR_TIMEOUT) if a kernel wait gave up."""
     _check(library().dflash2_check_device_status(workspace.ptr, workspace.nbytes, _stream(stream)),
            "dflash2_check_device_status")
 
 
+@_on_stream
 def dflash2_selftest_wait_timeout(workspace: Workspace, limit_us: int, stream=None) -> None:
     """Enqueue the bounded-wait self-test: a device wait that nothing satisfies gives up after
     limit_us and raises the workspace's status word (read it with dflash2_check_device_status)."""
